@@ -1,0 +1,477 @@
+"""Benchmark: draft tokens verified per second per SSM layer, and achieved HBM
+bandwidth of the fused verify/commit kernel against the B300 roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 3] [--cpu-seconds 10] [--no-cpu-baseline]
+
+A step is one pass of the whole path over one batch: for every layer of the
+workload one fused verify+commit launch (plain decode: one step launch).
+The default workload is the batched speculative-serving load (64 sequences,
+one Llama-3-8B-shaped layer: H 32, P 128, N 128, G 8, K 8, bf16 inputs, fp32
+state). Inputs are seeded synthetic data drawn on the CPU and resident in HBM
+before the timed region; steps rotate over several independent input sets
+whose total exceeds twice the L2, so no step reads another step's data from
+L2. Each step replays a CUDA graph of its launches; CUDA events on the
+launching stream time the whole region and every launch.
+
+Under torchrun every rank runs its own sequences (weak scaling, no collective
+in the data path); the elapsed time is the maximum over ranks.
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on
+bounded samples of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from ssm_recurrence_verify_b300 import synth  # noqa: E402
+
+L2_BYTES = 126 * 1000 * 1000
+HBM_SPEC_GBS = 8000.0
+FALLBACK_HBM_GBS = 6400.0
+METRIC = "draft tokens verified/s per SSM layer; achieved HBM GB/s vs B300 peak"
+KERNEL_SRC = os.path.join(ROOT, "ssm_recurrence_verify_b300", "csrc", "ssmverify.cu")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------------------- distributed host logic
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard(batch_per_rank: int, rank: int):
+    """Weak scaling: rank r owns sequences [r * batch, (r + 1) * batch)."""
+    return batch_per_rank, rank * batch_per_rank
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- bytes per launch
+
+def algorithmic_bytes(wl: synth.Workload, batch: int, accepted_nonzero: int) -> int:
+    """What one layer-call must move: the state read once, written only for
+    sequences with j > 0, x/B/C/dt read once (B/C once per group), y written
+    once in fp32, accept_len read."""
+    H, P, N, G, K = wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.ntok
+    eb = wl.in_elem_bytes()
+    slice_b = H * P * N * 4
+    return (batch * slice_b + accepted_nonzero * slice_b + batch * K * (H * P * eb + 2 * G * N * eb + H * eb)
+            + batch * K * H * P * 4 + (0 if wl.accept == "all" else batch * 4))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Polls the SM clock and clock-event reasons through NVML in a thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x40: "sw_thermal_slowdown",
+               0x80: "hw_thermal_slowdown", 0x100: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.02):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # pragma: no cover - depends on the host
+            self.err = str(e)
+
+    def _reasons(self):
+        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return int(f(self.h))
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append((time.perf_counter(), self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM),
+                                     self._reasons()))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self, t0: float, t1: float):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"nvml unavailable: {self.err}"}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "sampled during the timed region"
+        if not inside:
+            inside = self.samples
+            note = "timed region shorter than the sampling period: samples span warm-up and timed region"
+        mhz = [s[1] for s in inside]
+        bits = 0
+        for s in inside:
+            bits |= s[2]
+        reasons = sorted(name for bit, name in self.REASONS.items() if bits & bit)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ----------------------------------------------------------------------------- measured peaks / traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from a committed ncu capture of this kernel on
+    this workload, or None if absent or taken on different kernel source."""
+    path = os.path.join(PROFILES, f"ssm_scan_kernel_{workload_name}.traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class LayerSet:
+    """One independent input set: per layer the state, inputs, y and status."""
+
+    def __init__(self, wl, batch, offset, rnd, dev, layers):
+        self.layers = []
+        for layer in range(layers):
+            d = synth.draw_layer_round(wl, rnd=rnd, layer=layer, batch=batch, batch_offset=offset)
+            e = {k: v.to(dev) for k, v in d.items()}
+            e["y"] = torch.empty((batch, wl.ntok, wl.nheads, wl.headdim), dtype=torch.float32, device=dev)
+            e["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+            e["host"] = d
+            e["accepted_nonzero"] = int((d["accept_len"] > 0).sum())
+            self.layers.append(e)
+
+
+def launch_layer(ssm, wl, e):
+    if wl.accept == "all" and wl.ntok == 1:
+        ssm.step(e["state0"], e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], y=e["y"])
+    else:
+        ssm.verify_commit(e["state0"], e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], e["accept_len"], y=e["y"],
+                          dev_status=e["status"])
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import ssm_recurrence_verify_b300 as ssm
+    from ssm_recurrence_verify_b300 import build as libbuild
+    if not os.path.exists(libbuild.LIB):
+        libbuild.build()
+    ssm.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    batch, offset = shard(wl.batch, rank)
+    nl = wl.nlayers
+    step_bytes_est = nl * (2 * batch * wl.nheads * wl.headdim * wl.dstate * 4)
+    nsets = 1 if step_bytes_est >= 4 * L2_BYTES else max(3, math.ceil(2 * L2_BYTES / step_bytes_est) + 1)
+    sets = [LayerSet(wl, batch, offset, rnd, dev, nl) for rnd in range(nsets)]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    # eager warm-up of every set, then one CUDA graph per set
+    with torch.cuda.stream(stream):
+        for s in sets:
+            for e in s.layers:
+                launch_layer(ssm, wl, e)
+    torch.cuda.synchronize()
+    graphs = []
+    for s in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for e in s.layers:
+                launch_layer(ssm, wl, e)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % nsets].replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        t_all0.record(stream)
+        for i in range(K):
+            starts[i].record(stream)
+            graphs[(args.warmup + i) % nsets].replay()
+            ends[i].record(stream)
+        t_all1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    barrier(world)
+    sampler.stop()
+    elapsed_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
+    for s in sets:
+        for e in s.layers:
+            assert int(e["status"].item()) == 0, "device reported a bad accept_len"
+    max_ms = max_over_ranks(elapsed_ms, world)
+
+    # per-step algorithmic bytes, averaged over the sets the timed steps used
+    step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
+    used = [step_bytes[(args.warmup + i) % nsets] for i in range(K)]
+    mean_launch_bytes = statistics.fmean(used) / nl
+    mean_launch_ms = statistics.fmean(launch_ms) / nl
+    achieved = mean_launch_bytes / (mean_launch_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    tokens_per_step = batch * wl.ntok * world  # per layer: every rank's sequences x draft tokens
+    value = tokens_per_step * K / (max_ms * 1e-3)
+
+    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 else None
+    return {
+        "value": value, "ms_per_step": max_ms / K, "elapsed_ms": max_ms, "wall_s": wall1 - wall0,
+        "launch_ms_mean": mean_launch_ms, "launch_ms_median": statistics.median(launch_ms) / nl,
+        "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "bytes_per_launch": mean_launch_bytes,
+        "clocks": sampler.summary(wall0, wall1), "nsets": nsets, "e2e": e2e, "launches": K * nl,
+        "batch": batch,
+    }
+
+
+def run_e2e(ssm, args, wl, s, stream, dev, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads y back."""
+    keys = ("x", "B", "C", "dt") if wl.accept == "all" else ("x", "B", "C", "dt", "accept_len")
+    host = []
+    for e in s.layers:
+        h = {k: e["host"][k].pin_memory() for k in keys}
+        h["y"] = torch.empty(e["y"].shape, dtype=torch.float32).pin_memory()
+        host.append(h)
+    h2d = sum(sum(h[k].numel() * h[k].element_size() for k in keys) for h in host)
+    d2h = sum(h["y"].numel() * 4 for h in host)
+
+    def one_step():
+        for e, h in zip(s.layers, host):
+            for k in keys:
+                e[k].copy_(h[k], non_blocking=True)
+            launch_layer(ssm, wl, e)
+            h["y"].copy_(e["y"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one_step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = args.e2e_steps
+    barrier(world)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(n):
+            one_step()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    return {"value": s.layers[0]["x"].shape[0] * wl.ntok * world * n / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) legs
+
+def oracle_throughput(wl, seconds: float, max_seqs: int = None):
+    """Time the fp64 oracle (single thread, as it stands) on the workload's
+    first layer, repeating full passes over `max_seqs` sequences until
+    `seconds` have elapsed. Returns (tokens per second, description)."""
+    import oracle
+    seqs = wl.batch if max_seqs is None else min(wl.batch, max_seqs)
+    d = synth.draw_layer_round(wl, batch=seqs)
+    args = (d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"],
+            None if wl.accept == "all" else d["accept_len"])
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.verify_commit(*args)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    toks = seqs * wl.ntok * reps
+    return toks / el, (f"{reps} full oracle pass(es) over {seqs} sequence(s) x {wl.ntok} draft tokens of one layer "
+                       f"({wl.nheads} heads, P {wl.headdim}, N {wl.dstate}), fp64, {el:.1f} s")
+
+
+def reference_sample(wl, per_unit_s: float, steps: int):
+    """Pick (sequences, heads) per oracle step so that `steps` steps take
+    about two minutes. The smallest unit is one sequence and one B/C group's
+    heads; heads are taken as whole groups from head 0."""
+    hpg = wl.nheads // wl.ngroups
+    units_total = wl.batch * wl.ngroups
+    budget_units = 120.0 / max(1, steps) / per_unit_s
+    units = int(max(1, min(units_total, budget_units)))
+    if units >= wl.ngroups:
+        return min(wl.batch, units // wl.ngroups), wl.nheads
+    return 1, units * hpg
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    hpg = wl.nheads // wl.ngroups
+
+    def inputs(seqs, heads):
+        d = synth.draw_layer_round(wl, batch=seqs)
+        g = heads // hpg
+        return (d["state0"][:, :heads].contiguous(), d["x"][:, :, :heads].contiguous(),
+                d["B"][:, :, :g].contiguous(), d["C"][:, :, :g].contiguous(), d["dt"][:, :, :heads].contiguous(),
+                d["A"][:heads].contiguous(), d["D"][:heads].contiguous(),
+                None if wl.accept == "all" else d["accept_len"])
+
+    a1 = inputs(1, hpg)
+    t0 = time.perf_counter()
+    oracle.verify_commit(*a1)
+    per_unit = max(time.perf_counter() - t0, 1e-5)
+    seqs, heads = reference_sample(wl, per_unit, args.steps + args.warmup)
+    a = inputs(seqs, heads)
+    for _ in range(args.warmup):
+        oracle.verify_commit(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify_commit(*a)
+    el = time.perf_counter() - t0
+    # a token of one layer is all heads of one sequence; a head subset counts pro rata
+    value = seqs * wl.ntok * (heads / wl.nheads) * args.steps / el
+    sample = (f"each step: {seqs} of {wl.batch} sequences x {heads} of {wl.nheads} heads x {wl.ntok} draft tokens "
+              f"of one layer, fp64 oracle, single thread; tokens credited pro rata to the heads run")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
+        "config": workload_config(wl, None),
+        "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": 1, "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, nsets):
+    cfg = {"workload": wl.name, "batch_per_gpu": wl.batch, "layers": wl.nlayers, "nheads": wl.nheads,
+           "headdim": wl.headdim, "dstate": wl.dstate, "ngroups": wl.ngroups, "draft_tokens": wl.ntok,
+           "in_dtype": wl.in_dtype, "state_dtype": "f32", "accept_len": wl.accept, "parallelism": "replicas"}
+    if nsets is not None:
+        cfg["l2"] = (f"{nsets} independent input sets rotated; each set is read again only after more than "
+                     f"2x the 126 MB L2 of other traffic")
+        cfg["timing"] = "one CUDA graph replay per step, CUDA events on the launching stream"
+    return cfg
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = synth.WORKLOADS[args.workload]
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_ours(args, wl, rank, world, local_rank)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample = oracle_throughput(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        traffic = recorded_traffic(wl.name)
+        line = {
+            "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
+            "config": workload_config(wl, r["nsets"]),
+            "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": r["peak"], "unit": "GB/s",
+                         "frac": r["achieved_gbs"] / r["peak"], "traffic": traffic,
+                         "peak_source": f"{r['peak_kind']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                         "algorithmic_bytes_per_launch": r["bytes_per_launch"],
+                         "launch_us_mean": r["launch_ms_mean"] * 1e3,
+                         "frac_of_8tbs_spec": r["achieved_gbs"] / HBM_SPEC_GBS},
+            "cpu_baseline": cpu,
+            "e2e": r["e2e"],
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

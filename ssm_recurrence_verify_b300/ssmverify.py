@@ -1,0 +1,187 @@
+"""Python binding of libssmverify (ctypes): argument marshalling only.
+
+Every step of the path runs in the CUDA library; this module checks torch
+tensors (device, dtype, shape, contiguity), fills the C descriptor and calls
+the C ABI on the current CUDA stream. If the library is not built the first
+call raises: there is no fallback.
+
+Layouts (see ``include/ssmverify.h``): ``state[b][H][P][N]`` fp32,
+``x[b][K][H][P]``, ``B``/``C[b][K][G][N]``, ``dt[b][K][H]`` (fp32 or bf16, all
+the same), ``A``/``D[H]`` fp32, ``y[b][K][H][P]`` fp32, ``accept_len[b]`` int32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssmverify.so")
+
+SSM_F32 = 0
+SSM_BF16 = 1
+SSM_OK = 0
+SSM_ERR_NULL = 1
+SSM_ERR_SHAPE = 2
+SSM_ERR_UNSUPPORTED = 3
+SSM_ERR_ALIGN = 4
+SSM_ERR_ALIAS = 5
+SSM_ERR_CUDA = 6
+SSM_STATUS_BAD_ACCEPT_LEN = 1
+
+EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_step", "ssm_strerror",
+           "ssm_last_cuda_error", "ssm_version")
+
+
+class SsmDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
+                ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("ntok", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class SsmError(ValueError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libssmverify error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (once) and return the CUDA library; raise if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libssmverify is not built ({p} missing); run "
+                           "`python -m ssm_recurrence_verify_b300.build`")
+    lib = ctypes.CDLL(p)
+    vp, dp = ctypes.c_void_p, ctypes.POINTER(SsmDesc)
+    lib.ssm_verify.argtypes = [dp] + [vp] * 9
+    lib.ssm_commit.argtypes = [dp] + [vp] * 8
+    lib.ssm_verify_commit.argtypes = [dp] + [vp] * 11
+    lib.ssm_step.argtypes = [dp] + [vp] * 9
+    for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_step", "ssm_last_cuda_error", "ssm_version"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.ssm_strerror.argtypes = [ctypes.c_int]
+    lib.ssm_strerror.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load_library().ssm_strerror(code).decode()
+
+
+def _check(code: int):
+    if code != SSM_OK:
+        msg = strerror(code)
+        if code == SSM_ERR_CUDA:
+            msg += f" (cudaError {load_library().ssm_last_cuda_error()})"
+        raise SsmError(code, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _in_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise ValueError(f"x/B/C/dt must be float32 or bfloat16, got {t.dtype}")
+
+
+def make_desc(state_shape, x_shape, B_shape, in_dtype: int) -> SsmDesc:
+    bsz, H, P, N = state_shape
+    K = x_shape[1]
+    G = B_shape[2]
+    return SsmDesc(bsz, H, P, N, G, K, in_dtype, 0)
+
+
+def _validate(state, x, B, C, dt, A, D, accept_len, y):
+    tensors = {"state": state, "x": x, "B": B, "dt": dt, "A": A}
+    for k, v in (("C", C), ("D", D), ("accept_len", accept_len), ("y", y)):
+        if v is not None:
+            tensors[k] = v
+    dev = state.device
+    for k, v in tensors.items():
+        if not v.is_cuda or v.device != dev:
+            raise ValueError(f"{k} must be a CUDA tensor on {dev}")
+        if not v.is_contiguous():
+            raise ValueError(f"{k} must be contiguous")
+    if state.dtype != torch.float32 or state.dim() != 4:
+        raise ValueError("state must be float32 [batch][H][P][N]")
+    bsz, H, P, N = state.shape
+    if x.dim() != 4 or x.shape[0] != bsz or x.shape[2] != H or x.shape[3] != P:
+        raise ValueError(f"x must be [batch][K][H][P] = [{bsz}][K][{H}][{P}], got {tuple(x.shape)}")
+    K = x.shape[1]
+    if B.dim() != 4 or B.shape[0] != bsz or B.shape[1] != K or B.shape[3] != N:
+        raise ValueError(f"B must be [batch][K][G][N], got {tuple(B.shape)}")
+    G = B.shape[2]
+    if C is not None and tuple(C.shape) != tuple(B.shape):
+        raise ValueError("C must have B's shape")
+    if tuple(dt.shape) != (bsz, K, H):
+        raise ValueError(f"dt must be [batch][K][H] = [{bsz}][{K}][{H}], got {tuple(dt.shape)}")
+    dts = {x.dtype, B.dtype, dt.dtype} | ({C.dtype} if C is not None else set())
+    if len(dts) != 1:
+        raise ValueError("x, B, C, dt must share one dtype")
+    for k, v in (("A", A), ("D", D)):
+        if v is not None and (v.dtype != torch.float32 or tuple(v.shape) != (H,)):
+            raise ValueError(f"{k} must be float32 [H]")
+    if accept_len is not None and (accept_len.dtype != torch.int32 or tuple(accept_len.shape) != (bsz,)):
+        raise ValueError("accept_len must be int32 [batch]")
+    if y is not None and (y.dtype != torch.float32 or tuple(y.shape) != (bsz, K, H, P)):
+        raise ValueError("y must be float32 [batch][K][H][P]")
+    return make_desc(state.shape, x.shape, B.shape, _in_dtype(x)), G
+
+
+def _new_y(state, x):
+    bsz, K, H, P = x.shape
+    return torch.empty((bsz, K, H, P), dtype=torch.float32, device=state.device)
+
+
+def verify(state, x, B, C, dt, A, D, y=None, stream=None) -> torch.Tensor:
+    """y for all K draft tokens from the cached state; the state is only read."""
+    y = _new_y(state, x) if y is None else y
+    desc, _ = _validate(state, x, B, C, dt, A, D, None, y)
+    _check(load_library().ssm_verify(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
+                                     _ptr(D), _ptr(y), _stream(stream)))
+    return y
+
+
+def commit(state, x, B, dt, A, accept_len, dev_status=None, stream=None) -> None:
+    """Advance the state in place by each sequence's accepted prefix (j = 0: unchanged)."""
+    desc, _ = _validate(state, x, B, None, dt, A, None, accept_len, None)
+    _check(load_library().ssm_commit(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(dt), _ptr(A),
+                                     _ptr(accept_len), _ptr(dev_status), _stream(stream)))
+
+
+def verify_commit(state, x, B, C, dt, A, D, accept_len, y=None, dev_status=None, stream=None) -> torch.Tensor:
+    """Fused verify + commit: y for all K tokens, state <- h_j in place."""
+    y = _new_y(state, x) if y is None else y
+    desc, _ = _validate(state, x, B, C, dt, A, D, accept_len, y)
+    _check(load_library().ssm_verify_commit(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
+                                            _ptr(A), _ptr(D), _ptr(accept_len), _ptr(y), _ptr(dev_status),
+                                            _stream(stream)))
+    return y
+
+
+def step(state, x, B, C, dt, A, D, y=None, stream=None) -> torch.Tensor:
+    """Plain decode of one token (K = 1): y, and the state advanced in place."""
+    y = _new_y(state, x) if y is None else y
+    desc, _ = _validate(state, x, B, C, dt, A, D, None, y)
+    _check(load_library().ssm_step(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
+                                   _ptr(D), _ptr(y), _stream(stream)))
+    return y

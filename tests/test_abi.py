@@ -1,0 +1,196 @@
+"""The C ABI on the host: the library loads, exports what the header
+declares, and rejects bad arguments before launching anything.
+
+The fake-pointer cases never reach a launch (every one fails host
+validation); they still run only where no CUDA device is present, so that a
+validation bug could never hand a fake pointer to a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from ssm_recurrence_verify_b300 import build as libbuild
+from ssm_recurrence_verify_b300 import ssmverify as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssmverify.h")
+
+no_gpu_only = pytest.mark.skipif(torch.cuda.is_available(), reason="fake-pointer checks run on CPU-only hosts")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return sv.load_library()
+
+
+def header_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", txt)))
+
+
+def header_defines():
+    out = {}
+    for m in re.finditer(r"#define\s+(SSM_[A-Z0-9_]+)\s+(\d+)u?", open(HEADER).read()):
+        out[m.group(1)] = int(m.group(2))
+    return out
+
+
+def test_header_is_plain_c_and_cxx():
+    for lang in ("c", "c++"):
+        subprocess.check_call(["gcc", "-fsyntax-only", "-Wall", "-Werror", "-x", lang, HEADER])
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = header_functions()
+    assert set(declared) == set(sv.EXPORTS), declared
+    out = subprocess.run(["nm", "-D", "--defined-only", libbuild.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (ssm_[a-z_]+)\b", out))
+    for name in declared:
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_constants_match_header(lib):
+    d = header_defines()
+    for k, v in d.items():
+        if hasattr(sv, k):
+            assert getattr(sv, k) == v, k
+    assert lib.ssm_version() == d["SSM_VERSION"]
+    assert ctypes.sizeof(sv.SsmDesc) == 32
+
+
+def test_strerror(lib):
+    for code in range(0, 7):
+        s = sv.strerror(code)
+        assert isinstance(s, str) and s
+    assert sv.strerror(99) == "unknown error code"
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        sv.load_library(str(tmp_path / "missing.so"))
+
+
+# ----------------------------------------------------------------------------- host validation
+
+BASE = 1 << 40  # fake, never dereferenced: every call below fails validation
+
+
+def desc(**kw):
+    d = dict(batch=2, nheads=4, headdim=32, dstate=128, ngroups=2, ntok=3, in_dtype=sv.SSM_BF16, reserved=0)
+    d.update(kw)
+    return sv.SsmDesc(**d)
+
+
+def ptrs(n, start=BASE, gap=1 << 30):
+    return [ctypes.c_void_p(start + i * gap) for i in range(n)]
+
+
+def vc(lib, d, p):
+    """ssm_verify_commit(desc, state, x, B, C, dt, A, D, accept_len, y, dev_status, stream)."""
+    return lib.ssm_verify_commit(ctypes.byref(d) if d is not None else None, *p, None)
+
+
+@no_gpu_only
+def test_null_desc_and_pointers(lib):
+    assert vc(lib, None, ptrs(10)) == sv.SSM_ERR_NULL
+    for i in range(9):  # state, x, B, C, dt, A, D, accept_len, y are required
+        p = ptrs(10)
+        p[i] = None
+        assert vc(lib, desc(), p) == sv.SSM_ERR_NULL, i
+    p = ptrs(10)
+    p[9] = None  # dev_status is optional
+    # every pointer valid and distinct, but one misaligned -> still rejected before launch
+    p[0] = ctypes.c_void_p(BASE + 8)
+    assert vc(lib, desc(), p) == sv.SSM_ERR_ALIGN
+
+
+@no_gpu_only
+@pytest.mark.parametrize("field,value,code", [
+    ("batch", -1, sv.SSM_ERR_SHAPE), ("nheads", 0, sv.SSM_ERR_SHAPE), ("headdim", 0, sv.SSM_ERR_SHAPE),
+    ("ngroups", 3, sv.SSM_ERR_SHAPE), ("ngroups", 0, sv.SSM_ERR_SHAPE), ("ntok", 0, sv.SSM_ERR_SHAPE),
+    ("reserved", 1, sv.SSM_ERR_SHAPE), ("dstate", 96, sv.SSM_ERR_UNSUPPORTED), ("dstate", 512, sv.SSM_ERR_UNSUPPORTED),
+    ("dstate", 8, sv.SSM_ERR_UNSUPPORTED), ("in_dtype", 7, sv.SSM_ERR_UNSUPPORTED),
+])
+def test_shape_errors(lib, field, value, code):
+    d = desc(**{field: value})
+    p = ptrs(10)
+    p[0] = ctypes.c_void_p(BASE + 8)  # also misaligned: the shape check must come first
+    assert vc(lib, d, p) == code
+
+
+@no_gpu_only
+def test_alignment_errors(lib):
+    for i, off in [(0, 4), (1, 1), (2, 1), (3, 1), (4, 1), (5, 2), (6, 2), (7, 2), (8, 2), (9, 2)]:
+        p = ptrs(10)
+        p[i] = ctypes.c_void_p(p[i].value + off)
+        assert vc(lib, desc(), p) == sv.SSM_ERR_ALIGN, i
+    p = ptrs(10)
+    p[1] = ctypes.c_void_p(p[1].value + 2)  # 2-byte aligned is enough for bf16 ...
+    p[0] = ctypes.c_void_p(p[0].value + 16)
+    p[8] = ctypes.c_void_p(p[8].value + 4)
+    d = desc(in_dtype=sv.SSM_F32)  # ... but not for fp32 inputs
+    assert vc(lib, d, p) == sv.SSM_ERR_ALIGN
+
+
+@no_gpu_only
+def test_alias_errors(lib):
+    # state (written) overlapping x
+    p = ptrs(10)
+    p[1] = ctypes.c_void_p(p[0].value + 64)
+    assert vc(lib, desc(), p) == sv.SSM_ERR_ALIAS
+    # y (written) overlapping C
+    p = ptrs(10)
+    p[8] = ctypes.c_void_p(p[3].value + 16)
+    assert vc(lib, desc(), p) == sv.SSM_ERR_ALIAS
+    # two read-only buffers may overlap (B and C the same): validation passes
+    # and, with no CUDA device on this host, the launch itself fails
+    p = ptrs(10)
+    p[3] = p[2]
+    assert vc(lib, desc(), p) == sv.SSM_ERR_CUDA
+    assert lib.ssm_last_cuda_error() != 0
+    # dev_status inside y
+    p = ptrs(10)
+    p[9] = ctypes.c_void_p(p[8].value + 4)
+    assert vc(lib, desc(), p) == sv.SSM_ERR_ALIAS
+    # verify: the state is read only, so it may overlap inputs, but not y
+    d = desc()
+    q = ptrs(8)
+    q[7] = ctypes.c_void_p(q[0].value + 128)
+    assert lib.ssm_verify(ctypes.byref(d), *q, None) == sv.SSM_ERR_ALIAS
+
+
+@no_gpu_only
+def test_entry_specific_rules(lib):
+    d = desc()
+    p = ptrs(10)
+    p[7] = None
+    assert vc(lib, d, p) == sv.SSM_ERR_NULL        # verify_commit needs accept_len
+    q = ptrs(9)                                   # step: ntok must be 1
+    assert lib.ssm_step(ctypes.byref(d), *q, None) == sv.SSM_ERR_SHAPE
+    c = ptrs(7)                                   # commit: accept_len required
+    c[5] = None
+    assert lib.ssm_commit(ctypes.byref(d), *c, None) == sv.SSM_ERR_NULL
+
+
+@no_gpu_only
+def test_empty_batch_is_a_noop(lib):
+    d = desc(batch=0)
+    assert vc(lib, d, [None] * 10) == sv.SSM_OK
+    assert lib.ssm_verify(ctypes.byref(d), *([None] * 8), None) == sv.SSM_OK
+    assert lib.ssm_commit(ctypes.byref(d), *([None] * 7), None) == sv.SSM_OK
+    d1 = desc(batch=0, ntok=1)
+    assert lib.ssm_step(ctypes.byref(d1), *([None] * 8), None) == sv.SSM_OK
+
+
+def test_python_shim_rejects_cpu_tensors():
+    t = torch.zeros(1, 2, 16, 16)
+    x = torch.zeros(1, 1, 2, 16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sv.verify(t, x, torch.zeros(1, 1, 1, 16), torch.zeros(1, 1, 1, 16), torch.zeros(1, 1, 2), torch.zeros(2),
+                  torch.zeros(2), y=torch.zeros(1, 1, 2, 16))

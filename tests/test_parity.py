@@ -1,0 +1,165 @@
+"""GPU (through the C ABI) against the fp64 oracle, element by element.
+
+Every workload (the five synthetic configurations at full size; the 64-layer
+stack on four of its layers), plus ragged shapes, all dstate variants, chunk
+boundaries of the draft length, G = 1 and G = H, and the degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssm_recurrence_verify_b300 as ssm
+from gpu_helpers import RTOL_STATE, np64, rel_err, to_dev, y_tol
+from ssm_recurrence_verify_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_round(state64, t, p, acc):
+    return oracle.verify_commit(state64, t["x"], t["B"], t["C"], t["dt"], p["A"], p["D"], acc)
+
+
+def _check(y_gpu, st_gpu, ref, in_dtype, what):
+    ey = rel_err(np64(y_gpu), ref["y"])
+    es = rel_err(np64(st_gpu), ref["state"])
+    assert ey <= y_tol(in_dtype), f"{what}: y rel err {ey:.3e}"
+    assert es <= RTOL_STATE, f"{what}: state rel err {es:.3e}"
+
+
+def run_workload(wl, dev, layers=None, rounds=None):
+    """verify_commit over rounds x layers with the state carried across rounds;
+    each layer-call checked against the oracle fed the same inputs."""
+    layers = range(wl.nlayers) if layers is None else layers
+    rounds = wl.rounds if rounds is None else rounds
+    for layer in layers:
+        p = synth.draw_params(wl, layer)
+        st = p["state0"].to(dev)
+        s64 = p["state0"].double().numpy()
+        Ad, Dd = p["A"].to(dev), p["D"].to(dev)
+        for rnd in range(rounds):
+            t = synth.draw_tokens(wl, rnd, layer)
+            acc = synth.draw_accept_len(wl, rnd)
+            td = to_dev(t, dev)
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+            if wl.accept == "all" and wl.ntok == 1:
+                y = ssm.step(st, td["x"], td["B"], td["C"], td["dt"], Ad, Dd)
+                ref = oracle.verify_commit(s64, t["x"], t["B"], t["C"], t["dt"], p["A"], p["D"], None)
+            else:
+                y = ssm.verify_commit(st, td["x"], td["B"], td["C"], td["dt"], Ad, Dd, acc.to(dev),
+                                      dev_status=status)
+                ref = _oracle_round(s64, t, p, acc)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            _check(y, st, ref, wl.torch_in_dtype, f"{wl.name} layer {layer} round {rnd}")
+            s64 = ref["state"]  # each side carries its own state; the oracle keeps fp64
+
+
+def test_tiny_fp32_workload(cuda_device):
+    run_workload(synth.WORKLOADS[0], cuda_device)
+
+
+def test_tiny_fp32_workload_groups_equal_heads(cuda_device):
+    wl = synth.custom_workload(1, 2, 16, 16, 2, 4, synth.F32, seed=100)
+    run_workload(wl, cuda_device, rounds=3)
+
+
+def test_llama3_layer_decode(cuda_device):
+    run_workload(synth.WORKLOADS[1], cuda_device, rounds=4)
+
+
+def test_hybrid_16_layer_verify(cuda_device):
+    run_workload(synth.WORKLOADS[2], cuda_device)
+
+
+def test_batched_speculative_serving(cuda_device):
+    """The benchmark's workload at full size (batch 64, K 8), every output."""
+    run_workload(synth.WORKLOADS[3], cuda_device)
+
+
+def test_mamba2_stack_sampled_layers(cuda_device):
+    """The 64-layer stack at full per-layer size, on layers 0, 21, 42, 63."""
+    run_workload(synth.WORKLOADS[4], cuda_device, layers=[0, 21, 42, 63])
+
+
+SHAPES = [
+    # batch, H, P, N, G, K, dtype
+    (1, 2, 16, 16, 1, 4, synth.F32),
+    (2, 4, 50, 16, 4, 7, synth.BF16),       # ragged P, G = H
+    (3, 2, 33, 32, 1, 16, synth.F32),       # K exactly one chunk
+    (2, 3, 64, 32, 3, 17, synth.BF16),      # K crosses the chunk boundary
+    (2, 4, 100, 64, 2, 33, synth.F32),      # three chunks, ragged P
+    (1, 8, 128, 128, 8, 1, synth.BF16),
+    (5, 4, 129, 128, 1, 9, synth.BF16),     # one row past a tile
+    (2, 2, 7, 256, 1, 5, synth.F32),        # tiny P, widest N
+    (2, 2, 72, 256, 2, 12, synth.BF16),
+    (1, 1, 1, 128, 1, 3, synth.F32),        # a single row
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}h{}p{}n{}g{}k{}{}".format(*s))
+def test_shapes(cuda_device, shape):
+    wl = synth.custom_workload(*shape, seed=sum(shape[:6]))
+    run_workload(wl, cuda_device, rounds=2)
+
+
+def test_large_headdim(cuda_device):
+    """A long ragged head dimension (many row tiles)."""
+    wl = synth.custom_workload(1, 1, 4100, 256, 1, 3, synth.BF16, seed=77)
+    run_workload(wl, cuda_device, rounds=1)
+
+
+def test_verify_and_commit_unfused_match_oracle(cuda_device):
+    """The serving order: verify (state read only) then commit."""
+    wl = synth.custom_workload(4, 8, 128, 128, 2, 8, synth.BF16, seed=3)
+    d = synth.draw_layer_round(wl)
+    dd = to_dev(d, cuda_device)
+    before = dd["state0"].clone()
+    y = ssm.verify(dd["state0"], dd["x"], dd["B"], dd["C"], dd["dt"], dd["A"], dd["D"])
+    torch.cuda.synchronize()
+    assert torch.equal(before, dd["state0"])
+    ssm.commit(dd["state0"], dd["x"], dd["B"], dd["dt"], dd["A"], dd["accept_len"])
+    ref = oracle.verify_commit(d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], d["accept_len"])
+    _check(y, dd["state0"], ref, torch.bfloat16, "unfused")
+
+
+def test_zero_and_full_acceptance(cuda_device):
+    wl = synth.custom_workload(6, 4, 64, 128, 2, 6, synth.F32, seed=9)
+    d = synth.draw_layer_round(wl)
+    d["accept_len"] = torch.tensor([0, 6, 0, 6, 3, 1], dtype=torch.int32)
+    dd = to_dev(d, cuda_device)
+    y = ssm.verify_commit(dd["state0"], dd["x"], dd["B"], dd["C"], dd["dt"], dd["A"], dd["D"], dd["accept_len"])
+    ref = oracle.verify_commit(d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], d["accept_len"])
+    _check(y, dd["state0"], ref, torch.float32, "zero/full acceptance")
+    got = dd["state0"].cpu()
+    for b in (0, 2):
+        assert torch.equal(got[b], d["state0"][b])
+
+
+def test_empty_batch_noop(cuda_device):
+    e = torch.empty(0, 2, 16, 16, device=cuda_device)
+    x = torch.empty(0, 3, 2, 16, device=cuda_device)
+    B = torch.empty(0, 3, 1, 16, device=cuda_device)
+    dt = torch.empty(0, 3, 2, device=cuda_device)
+    A = torch.zeros(2, device=cuda_device)
+    acc = torch.empty(0, dtype=torch.int32, device=cuda_device)
+    y = ssm.verify_commit(e, x, B, B.clone(), dt, A, A.clone(), acc)
+    torch.cuda.synchronize()
+    assert y.shape == (0, 3, 2, 16)
+
+
+def test_sampled_slices_at_full_size(cuda_device):
+    """Property at full size, slice by slice: the benchmark's batch, with the
+    oracle run one (sequence, head) at a time on a spread of slices."""
+    wl = synth.WORKLOADS[3]
+    d = synth.draw_layer_round(wl, rnd=5)
+    dd = to_dev(d, cuda_device)
+    y = ssm.verify_commit(dd["state0"], dd["x"], dd["B"], dd["C"], dd["dt"], dd["A"], dd["D"], dd["accept_len"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    pairs = [(int(rng.integers(0, wl.batch)), int(rng.integers(0, wl.nheads))) for _ in range(24)]
+    ref = oracle.verify_commit_slices(d, pairs)
+    yc, sc = y.cpu(), dd["state0"].cpu()
+    for (b, h), r in ref.items():
+        assert rel_err(np64(yc[b, :, h]), r["y"]) <= y_tol(torch.bfloat16), (b, h)
+        assert rel_err(np64(sc[b, h]), r["state"]) <= RTOL_STATE, (b, h)
