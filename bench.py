@@ -92,59 +92,100 @@ def algorithmic_bytes(wl: synth.Workload, batch: int, accepted_nonzero: int) -> 
 
 # ----------------------------------------------------------------------------- clocks
 
+def physical_gpu(local_rank: int) -> str:
+    """The nvidia-smi / NVML id of this process's GPU (CUDA_VISIBLE_DEVICES aware)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
 class ClockSampler:
-    """Polls the SM clock and clock-event reasons through NVML in a thread."""
+    """Samples the SM clock and clock-event reasons during a window, through
+    NVML in a thread, or through a `nvidia-smi -lms` subprocess where the
+    NVML binding is not installed."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x40: "sw_thermal_slowdown",
                0x80: "hw_thermal_slowdown", 0x100: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
 
-    def __init__(self, index: int, period_s: float = 0.02):
-        self.samples = []
+    def __init__(self, local_rank: int, period_s: float = 0.02):
+        self.samples = []  # (perf_counter, sm_mhz, reason bits)
         self.period = period_s
-        self.ok = False
+        self.gpu = physical_gpu(local_rank)
+        self.max_mhz = None
+        self.err = ""
+        self.mode = None
         self._stop = threading.Event()
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.h = (pynvml.nvmlDeviceGetHandleByUUID(self.gpu) if self.gpu.startswith(("GPU-", "MIG-"))
+                      else pynvml.nvmlDeviceGetHandleByIndex(int(self.gpu)))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # pragma: no cover - depends on the host
-            self.err = str(e)
+            self.mode = "nvml"
+        except Exception as e:
+            self.err = f"nvml: {e}"
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _reasons(self):
+    def _nvml_loop(self):
         f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        return int(f(self.h))
-
-    def _run(self):
         while not self._stop.is_set():
             try:
                 self.samples.append((time.perf_counter(), self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM),
-                                     self._reasons()))
+                                     int(f(self.h))))
             except Exception:
                 pass
             time.sleep(self.period)
 
+    def _smi_loop(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                self.samples.append((time.perf_counter(), float(parts[0]), int(parts[2], 16)))
+                self.max_mhz = float(parts[1])
+            except ValueError:
+                continue
+
     def start(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
             self.t.start()
+        elif self.mode == "nvidia-smi":
+            import subprocess
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", str(int(self.period * 1000))],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.t = threading.Thread(target=self._smi_loop, daemon=True)
+            self.t.start()
+            time.sleep(0.3)  # let the first samples arrive
 
     def stop(self):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif self.mode == "nvidia-smi":
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait()
+            self.t.join(timeout=2)
 
     def summary(self, t0: float, t1: float):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"nvml unavailable: {self.err}"}
+        if self.mode is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"no clock source: {self.err}"}
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
-        note = "sampled during the timed region"
+        note = f"{self.mode}, sampled during the timed region"
         if not inside:
             inside = self.samples
-            note = "timed region shorter than the sampling period: samples span warm-up and timed region"
+            note = f"{self.mode}: timed region shorter than the sampling period; samples span warm-up and timed region"
         mhz = [s[1] for s in inside]
         bits = 0
         for s in inside:
