@@ -214,7 +214,7 @@ def kernel_source_hash() -> str:
 def recorded_traffic(workload_name: str):
     """DRAM bytes per launch from a committed ncu capture of this kernel on
     this workload, or None if absent or taken on different kernel source."""
-    path = os.path.join(PROFILES, f"ssm_scan_kernel_{workload_name}.traffic.json")
+    path = os.path.join(PROFILES, f"ssm_tile_kernel_{workload_name}.traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)

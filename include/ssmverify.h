@@ -36,24 +36,32 @@
  *
  * Ownership and threading: every pointer is a DEVICE pointer owned by the
  * caller (for the whole time the launched work runs). The library allocates
- * nothing, frees nothing, never synchronises and keeps no mutable global
- * state; every entry point only validates its arguments and enqueues one
- * kernel on `stream` (a cudaStream_t passed as void*, NULL = the legacy
- * default stream) on the current device. Calls are asynchronous.
+ * nothing, frees nothing and never synchronises; the only state it keeps
+ * between calls is a cache of immutable device properties (SM count and
+ * resident blocks per SM, per kernel and device), so calls are thread-safe.
+ * Every entry point only validates its arguments and enqueues one kernel on
+ * `stream` (a cudaStream_t passed as void*, NULL = the legacy default
+ * stream) on the current device. Calls are asynchronous.
  *
  * Errors: the return value is SSM_OK or an SSM_ERR_* code. Argument errors
  * are detected on the host before anything is launched (no device work is
  * enqueued then). SSM_ERR_CUDA reports a failed launch; the CUDA error code
  * of the calling thread's last failed launch is ssm_last_cuda_error().
- * Errors found on the device (an accept_len outside [0, ntok]) never trap:
- * the affected sequence's state is left untouched and, if dev_status is not
- * NULL, SSM_STATUS_BAD_ACCEPT_LEN is OR-ed into *dev_status, which the caller
- * reads after its own synchronisation.
+ * Errors found on the device never trap. An accept_len outside [0, ntok]
+ * leaves the affected sequence's state untouched and, if dev_status is not
+ * NULL, ORs SSM_STATUS_BAD_ACCEPT_LEN into *dev_status. A kernel block whose
+ * wait for its own state copy exceeds one second (which does not happen on a
+ * healthy device) stops early and ORs SSM_STATUS_TIMEOUT: its outputs are
+ * then incomplete. The caller reads *dev_status after its own
+ * synchronisation; it is only ever OR-ed into, so the caller zeroes it.
  *
  * Supported shapes: dstate in {16, 32, 64, 128, 256}; any headdim >= 1;
  * nheads % ngroups == 0; ntok >= 1; batch >= 0 (batch == 0 is a no-op that
  * inspects no pointer). Alignment: state 16 bytes; x, B, C, dt their element
- * size; A, D, y, accept_len, dev_status 4 bytes.
+ * size; A, D, y, accept_len, dev_status 4 bytes. x whose base is 16-byte
+ * aligned with headdim * element size a multiple of 16, and 16-byte aligned
+ * B / C, are read with 128-bit loads; other layouts take a scalar path with
+ * the same results.
  * Aliasing: a buffer the call writes (y; state for the committing calls) must
  * not overlap any other buffer of the call.
  */
@@ -83,6 +91,7 @@ extern "C" {
 
 /* bits OR-ed into *dev_status by the device */
 #define SSM_STATUS_BAD_ACCEPT_LEN 1u
+#define SSM_STATUS_TIMEOUT 2u
 
 typedef struct {
     int32_t batch;    /* sequences */
@@ -102,7 +111,7 @@ typedef struct {
  * y is produced for all K tokens because acceptance is decided from them.
  */
 int ssm_verify(const ssm_desc_t *desc, const float *state, const void *x, const void *B, const void *C,
-               const void *dt, const float *A, const float *D, float *y, void *stream);
+               const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
 
 /*
  * ssm_commit -- advance each sequence's cached state by its accepted prefix:
@@ -125,13 +134,35 @@ int ssm_verify_commit(const ssm_desc_t *desc, float *state, const void *x, const
                       uint32_t *dev_status, void *stream);
 
 /*
+ * ssm_commit_verify -- the serving order, where accept_len is known only
+ * after every layer has verified: commit the previous round's accepted
+ * prefix and verify the new draft tokens in one pass over the state (one
+ * read, one write). For each sequence, replay tokens 0 .. j-1 of the
+ * previous round's block (x_prev / B_prev / dt_prev, laid out like x / B /
+ * dt with prev_ntok tokens; j = accept_len_prev[b]), write h_j in place
+ * (nothing when j = 0), then run the desc->ntok new draft tokens from h_j and
+ * emit y for every one of them; the new drafts' states are not stored (they
+ * are committed by the next call). The result equals ssm_commit(previous
+ * block, accept_len_prev) followed by ssm_verify(new block), bit for bit.
+ * This is the speculative-decoding section's accept / roll back / continue
+ * loop with the state update deferred to the next round. An accept_len_prev
+ * outside [0, prev_ntok] replays nothing and writes nothing for that
+ * sequence (y is still produced) and sets SSM_STATUS_BAD_ACCEPT_LEN.
+ * prev_ntok >= 1; the previous block must not overlap the written buffers.
+ */
+int ssm_commit_verify(const ssm_desc_t *desc, float *state, int32_t prev_ntok, const void *x_prev,
+                      const void *B_prev, const void *dt_prev, const int32_t *accept_len_prev, const void *x,
+                      const void *B, const void *C, const void *dt, const float *A, const float *D, float *y,
+                      uint32_t *dev_status, void *stream);
+
+/*
  * ssm_step -- plain decoding, one token (desc->ntok must be 1): y for the
  * token and the state advanced by it in place. This is the ordinary decoding
  * that speculative decoding is compared against (results section of the news
  * summary).
  */
 int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B, const void *C,
-             const void *dt, const float *A, const float *D, float *y, void *stream);
+             const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
 
 /* A static, human-readable string for an SSM_* return code. */
 const char *ssm_strerror(int code);

@@ -30,8 +30,9 @@ SSM_ERR_ALIGN = 4
 SSM_ERR_ALIAS = 5
 SSM_ERR_CUDA = 6
 SSM_STATUS_BAD_ACCEPT_LEN = 1
+SSM_STATUS_TIMEOUT = 2
 
-EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_step", "ssm_strerror",
+EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step", "ssm_strerror",
            "ssm_last_cuda_error", "ssm_version")
 
 
@@ -61,11 +62,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                            "`python -m ssm_recurrence_verify_b300.build`")
     lib = ctypes.CDLL(p)
     vp, dp = ctypes.c_void_p, ctypes.POINTER(SsmDesc)
-    lib.ssm_verify.argtypes = [dp] + [vp] * 9
+    lib.ssm_verify.argtypes = [dp] + [vp] * 10
     lib.ssm_commit.argtypes = [dp] + [vp] * 8
     lib.ssm_verify_commit.argtypes = [dp] + [vp] * 11
-    lib.ssm_step.argtypes = [dp] + [vp] * 9
-    for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_step", "ssm_last_cuda_error", "ssm_version"):
+    lib.ssm_commit_verify.argtypes = [dp, vp, ctypes.c_int32] + [vp] * 13
+    lib.ssm_step.argtypes = [dp] + [vp] * 10
+    for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
+              "ssm_last_cuda_error", "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
     lib.ssm_strerror.restype = ctypes.c_char_p
@@ -152,12 +155,12 @@ def _new_y(state, x):
     return torch.empty((bsz, K, H, P), dtype=torch.float32, device=state.device)
 
 
-def verify(state, x, B, C, dt, A, D, y=None, stream=None) -> torch.Tensor:
+def verify(state, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
     """y for all K draft tokens from the cached state; the state is only read."""
     y = _new_y(state, x) if y is None else y
     desc, _ = _validate(state, x, B, C, dt, A, D, None, y)
     _check(load_library().ssm_verify(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
-                                     _ptr(D), _ptr(y), _stream(stream)))
+                                     _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
 
 
@@ -178,10 +181,35 @@ def verify_commit(state, x, B, C, dt, A, D, accept_len, y=None, dev_status=None,
     return y
 
 
-def step(state, x, B, C, dt, A, D, y=None, stream=None) -> torch.Tensor:
+def commit_verify(state, x_prev, B_prev, dt_prev, accept_len_prev, x, B, C, dt, A, D, y=None, dev_status=None,
+                  stream=None) -> torch.Tensor:
+    """Commit the previous round's accepted prefix (x_prev / B_prev / dt_prev,
+    accept_len_prev) into the state in place, then verify the new drafts from
+    it: y for every new token. Equals commit(...) then verify(...)."""
+    y = _new_y(state, x) if y is None else y
+    desc, G = _validate(state, x, B, C, dt, A, D, None, y)
+    bsz, H, P, N = state.shape
+    if x_prev.dim() != 4 or x_prev.shape[0] != bsz or x_prev.shape[2:] != (H, P):
+        raise ValueError(f"x_prev must be [batch][K_prev][H][P], got {tuple(x_prev.shape)}")
+    kp = x_prev.shape[1]
+    for k, v, shape in (("B_prev", B_prev, (bsz, kp, G, N)), ("dt_prev", dt_prev, (bsz, kp, H))):
+        if tuple(v.shape) != shape:
+            raise ValueError(f"{k} must be {list(shape)}, got {tuple(v.shape)}")
+    for k, v in (("x_prev", x_prev), ("B_prev", B_prev), ("dt_prev", dt_prev)):
+        if v.dtype != x.dtype or not v.is_cuda or v.device != state.device or not v.is_contiguous():
+            raise ValueError(f"{k} must be a contiguous {x.dtype} CUDA tensor on {state.device}")
+    if accept_len_prev.dtype != torch.int32 or tuple(accept_len_prev.shape) != (bsz,) or not accept_len_prev.is_cuda:
+        raise ValueError("accept_len_prev must be int32 [batch] on the GPU")
+    _check(load_library().ssm_commit_verify(ctypes.byref(desc), _ptr(state), kp, _ptr(x_prev), _ptr(B_prev),
+                                            _ptr(dt_prev), _ptr(accept_len_prev), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
+                                            _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def step(state, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
     """Plain decode of one token (K = 1): y, and the state advanced in place."""
     y = _new_y(state, x) if y is None else y
     desc, _ = _validate(state, x, B, C, dt, A, D, None, y)
     _check(load_library().ssm_step(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
-                                   _ptr(D), _ptr(y), _stream(stream)))
+                                   _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y

@@ -96,6 +96,12 @@ def vc(lib, d, p):
     return lib.ssm_verify_commit(ctypes.byref(d) if d is not None else None, *p, None)
 
 
+def cv(lib, d, prev_ntok, p):
+    """ssm_commit_verify(desc, state, prev_ntok, x_prev, B_prev, dt_prev, accept_len_prev, x, B, C, dt, A,
+    D, y, dev_status, stream); p holds the 13 pointers, state first (prev_ntok goes after it)."""
+    return lib.ssm_commit_verify(ctypes.byref(d) if d is not None else None, p[0], prev_ntok, *p[1:], None)
+
+
 @no_gpu_only
 def test_null_desc_and_pointers(lib):
     assert vc(lib, None, ptrs(10)) == sv.SSM_ERR_NULL
@@ -160,9 +166,12 @@ def test_alias_errors(lib):
     assert vc(lib, desc(), p) == sv.SSM_ERR_ALIAS
     # verify: the state is read only, so it may overlap inputs, but not y
     d = desc()
-    q = ptrs(8)
+    q = ptrs(9)
     q[7] = ctypes.c_void_p(q[0].value + 128)
     assert lib.ssm_verify(ctypes.byref(d), *q, None) == sv.SSM_ERR_ALIAS
+    q = ptrs(9)
+    q[1] = ctypes.c_void_p(q[0].value + 128)  # x inside the read-only state: allowed
+    assert lib.ssm_verify(ctypes.byref(d), *q, None) == sv.SSM_ERR_CUDA
 
 
 @no_gpu_only
@@ -182,10 +191,11 @@ def test_entry_specific_rules(lib):
 def test_empty_batch_is_a_noop(lib):
     d = desc(batch=0)
     assert vc(lib, d, [None] * 10) == sv.SSM_OK
-    assert lib.ssm_verify(ctypes.byref(d), *([None] * 8), None) == sv.SSM_OK
+    assert lib.ssm_verify(ctypes.byref(d), *([None] * 9), None) == sv.SSM_OK
     assert lib.ssm_commit(ctypes.byref(d), *([None] * 7), None) == sv.SSM_OK
+    assert cv(lib, d, 3, [None] * 13) == sv.SSM_OK
     d1 = desc(batch=0, ntok=1)
-    assert lib.ssm_step(ctypes.byref(d1), *([None] * 8), None) == sv.SSM_OK
+    assert lib.ssm_step(ctypes.byref(d1), *([None] * 9), None) == sv.SSM_OK
 
 
 def test_python_shim_rejects_cpu_tensors():
@@ -194,3 +204,31 @@ def test_python_shim_rejects_cpu_tensors():
     with pytest.raises(ValueError, match="CUDA tensor"):
         sv.verify(t, x, torch.zeros(1, 1, 1, 16), torch.zeros(1, 1, 1, 16), torch.zeros(1, 1, 2), torch.zeros(2),
                   torch.zeros(2), y=torch.zeros(1, 1, 2, 16))
+
+
+@no_gpu_only
+def test_commit_verify_validation(lib):
+    d = desc()
+    # state, x_prev, B_prev, dt_prev, accept_len_prev, x, B, C, dt, A, D, y, dev_status
+    p = ptrs(13)
+    for i in range(12):  # all but dev_status are required
+        q = list(p)
+        q[i] = None
+        assert cv(lib, d, 3, q) == sv.SSM_ERR_NULL, i
+    assert cv(lib, d, 0, p) == sv.SSM_ERR_SHAPE          # prev_ntok >= 1
+    assert cv(lib, d, -2, p) == sv.SSM_ERR_SHAPE
+    q = list(p)
+    q[1] = ctypes.c_void_p(q[1].value + 1)                # x_prev misaligned for bf16
+    assert cv(lib, d, 3, q) == sv.SSM_ERR_ALIGN
+    q = list(p)
+    q[0] = ctypes.c_void_p(q[0].value + 8)                # state needs 16 bytes
+    assert cv(lib, d, 3, q) == sv.SSM_ERR_ALIGN
+    q = list(p)
+    q[11] = ctypes.c_void_p(q[2].value + 64)              # y inside B_prev
+    assert cv(lib, d, 3, q) == sv.SSM_ERR_ALIAS
+    q = list(p)
+    q[1] = ctypes.c_void_p(q[0].value + 256)              # x_prev inside the written state
+    assert cv(lib, d, 3, q) == sv.SSM_ERR_ALIAS
+    q = list(p)
+    q[5] = q[1]                                           # the two blocks may share read-only buffers
+    assert cv(lib, d, 3, q) == sv.SSM_ERR_CUDA

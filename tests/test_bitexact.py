@@ -114,3 +114,22 @@ def test_repeat_is_deterministic(cuda_device):
         outs.append((s, y))
     torch.cuda.synchronize()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda s: "b{}h{}p{}n{}g{}k{}{}".format(*s))
+def test_commit_verify_equals_commit_then_verify(cuda_device, case):
+    """The deferred-commit kernel gives bit for bit the state of ssm_commit on
+    the previous block and the y of ssm_verify from that state."""
+    d, K = _inputs(case, cuda_device)
+    new = synth.custom_workload(case[0], case[1], case[2], case[3], case[4], max(1, K // 2 + 1), case[6],
+                                seed=3000 + K)
+    n = to_dev(synth.draw_tokens(new, 1), cuda_device)
+    s1 = d["state0"].clone()
+    y1 = ssm.commit_verify(s1, d["x"], d["B"], d["dt"], d["accept_len"], n["x"], n["B"], n["C"], n["dt"], d["A"],
+                           d["D"])
+    s2 = d["state0"].clone()
+    ssm.commit(s2, d["x"], d["B"], d["dt"], d["A"], d["accept_len"])
+    y2 = ssm.verify(s2, n["x"], n["B"], n["C"], n["dt"], d["A"], d["D"])
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2)
+    assert torch.equal(y1, y2)

@@ -36,6 +36,8 @@ def test_sentinels_untouched(cuda_device, shape):
     ssm.verify_commit(s, d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], d["accept_len"], y=y)
     ssm.verify(s, d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], y=y)
     ssm.commit(s, d["x"], d["B"], d["dt"], d["A"], d["accept_len"])
+    ssm.commit_verify(s, d["x"], d["B"], d["dt"], d["accept_len"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"],
+                      y=y)
     torch.cuda.synchronize()
     assert _intact(sbuf, s.numel())
     assert _intact(ybuf, y.numel())

@@ -163,3 +163,61 @@ def test_sampled_slices_at_full_size(cuda_device):
     for (b, h), r in ref.items():
         assert rel_err(np64(yc[b, :, h]), r["y"]) <= y_tol(torch.bfloat16), (b, h)
         assert rel_err(np64(sc[b, h]), r["state"]) <= RTOL_STATE, (b, h)
+
+
+def _serving_rounds(dev, wl_of_round, rounds, bad_round=None):
+    """The serving order with the commit deferred by one round: round 0 only
+    verifies; every later round commit_verify()s the previous round's accepted
+    prefix and verifies the new drafts. The oracle commits the previous block
+    (fp64), then computes the new drafts' y from that state."""
+    wl0 = wl_of_round(0)
+    p = synth.draw_params(wl0)
+    st = p["state0"].to(dev)
+    s64 = p["state0"].double().numpy()
+    Ad, Dd = p["A"].to(dev), p["D"].to(dev)
+    prev = None
+    for rnd in range(rounds):
+        wl = wl_of_round(rnd)
+        t = synth.draw_tokens(wl, rnd)
+        acc = synth.draw_accept_len(wl, rnd)
+        td = to_dev(t, dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if prev is None:
+            y = ssm.verify(st, td["x"], td["B"], td["C"], td["dt"], Ad, Dd, dev_status=status)
+        else:
+            pt, pacc = prev
+            if rnd == bad_round:
+                pacc = pacc.clone()
+                pacc[0] = -3
+            ptd = to_dev(pt, dev)
+            y = ssm.commit_verify(st, ptd["x"], ptd["B"], ptd["dt"], pacc.to(dev), td["x"], td["B"], td["C"],
+                                  td["dt"], Ad, Dd, dev_status=status)
+            s64 = oracle.verify_commit(s64, pt["x"], pt["B"], pt["C"], pt["dt"], p["A"], p["D"], pacc)["state"]
+        ref = oracle.verify_commit(s64, t["x"], t["B"], t["C"], t["dt"], p["A"], p["D"],
+                                   torch.zeros(wl.batch, dtype=torch.int32))
+        torch.cuda.synchronize()
+        want_status = ssm.ssmverify.SSM_STATUS_BAD_ACCEPT_LEN if rnd == bad_round else 0
+        assert int(status.item()) == want_status, rnd
+        ey = rel_err(np64(y), ref["y"])
+        es = rel_err(np64(st), s64)
+        assert ey <= y_tol(wl.torch_in_dtype), f"round {rnd}: y rel err {ey:.3e}"
+        assert es <= RTOL_STATE, f"round {rnd}: state rel err {es:.3e}"
+        prev = (t, acc)
+
+
+def test_commit_verify_serving_order(cuda_device):
+    """Five rounds of the deferred-commit serving order on the Llama-3-8B layer
+    shape (batch 4, K 8)."""
+    wl = synth.custom_workload(4, 32, 128, 128, 8, 8, synth.BF16, seed=31)
+    _serving_rounds(cuda_device, lambda r: wl, 5)
+
+
+def test_commit_verify_varying_draft_length(cuda_device):
+    """Draft lengths that change between rounds, across the staging chunk
+    (12 > 8 tokens), ragged P, fp32 inputs, and a bad accept_len in round 2
+    (that sequence replays nothing; status bit set; y still produced)."""
+    ks = [12, 3, 9, 1]
+
+    def wl_of(r):
+        return synth.custom_workload(3, 4, 50, 64, 2, ks[r], synth.F32, seed=32)
+    _serving_rounds(cuda_device, wl_of, len(ks), bad_round=2)
