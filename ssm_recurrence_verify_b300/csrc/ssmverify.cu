@@ -14,32 +14,35 @@
 // continuous-time SSM; C, B, x take the roles of Q, K, V).
 //
 // Kernel design (B300, bound by HBM traffic of the fp32 state):
-//  * Work unit = a tile of kRows head-dim rows p of one (b, h) state slice
-//    [P][N]: kRows * N * 4 contiguous bytes (32 KiB at N = 128).
+//  * Work unit = a tile of kRows head-dim rows of one (b, h) state slice
+//    [P][N] (64 rows x N, or 32 rows at N = 256): contiguous bytes.
 //  * Persistent grid: (SMs x resident CTAs) CTAs walk the tiles round-robin.
-//    While a CTA runs the token loop of one tile, the next tile's state is
-//    already streaming into shared memory through a 1-D TMA bulk copy
-//    (cp.async.bulk, completion on an mbarrier), so HBM never waits for the
-//    arithmetic. Waits on the mbarrier are bounded in time; a CTA that gives
-//    up records SSM_STATUS_TIMEOUT, drains its copy (again bounded) and exits.
-//  * The tile's state lives in registers for all tokens: 8 rows x 8 columns
-//    per thread. A row group of N/8 lanes spans one row set; lane l holds
-//    columns 4l..4l+3 and N/2+4l..N/2+4l+3, so every warp-wide 128-bit access
-//    covers whole 256-byte spans.
-//  * Per-token inputs are staged in shared memory kTC tokens at a time with
-//    vector loads issued together: Abar = exp(dt A), u = dt x, D x, B, C.
-//  * Update with paired fp32 instructions: h <- Abar * h + (u_p * B_n), two
-//    IEEE roundings per element, in one device function shared by every
-//    flavour, so fused, commit-only, replay and single-step paths agree bit
-//    for bit.
-//  * y_t[p] = sum_n C_t[n] h_t[p][n]: per-thread partial sums over its 8
-//    columns, then a transposing butterfly over the N/8 lanes of the row group
-//    (each level halves the rows a lane holds), then D x is added.
-//  * A launch runs up to two phases over each tile: a replay phase that
-//    advances the state over an accepted prefix of a replay block (no y), and
-//    a verify phase over the K draft tokens (y for every token). The state is
-//    written once: after the replay phase, or in the verify phase right after
-//    token j-1 (streaming stores straight from registers); j = 0 writes nothing.
+//    While a CTA works on one tile, the next tile's state and the raw x / B /
+//    C rows of its first kTC draft tokens stream into shared memory through
+//    1-D TMA bulk copies completing on one mbarrier, so HBM never waits for
+//    the arithmetic. Waits on the mbarrier are bounded in time; a CTA that
+//    gives up records SSM_STATUS_TIMEOUT, drains its copies and exits.
+//  * y from the attention-like (dual) form of the recurrence over a chunk of
+//    up to kTC tokens that starts from state h:
+//        y_t = w_t (C_t . h) + sum_{s<=t} L[t,s] (C_t . B_s) u_s + D x_t
+//        w_t = exp(A cs_t), L[t,s] = exp(A (cs_t - cs_s)), cs_t = sum_{r<=t} dt_r
+//    (C, B, x in the roles of Q, K, V: the correspondence the distillation
+//    starts from). h . C^T and C . B^T are dense contractions and run on the
+//    tensor cores (mma.sync m16n8k8 tf32, fp32 accumulation), with the
+//    fp32 operands split into a tf32 high part and a tf32 low part so that
+//    the products keep fp32 accuracy; bf16 inputs are exact in tf32 and need
+//    no split. The state stays in registers in the mma fragment layout: warp
+//    w owns 16 rows of the tile, a thread rows g and g + 8 and, of each 8
+//    columns, those the fragment gives it.
+//  * The state itself advances by the exact recurrence (h <- Abar h + u B,
+//    two IEEE roundings per element, paired fp32 instructions) only as far
+//    as needed: up to the committed token j (and through the chunk when
+//    more chunks follow). Every flavour shares that device function, so the
+//    fused, commit-only, deferred-commit and single-step paths agree bit for
+//    bit, and verify-only launches run no recurrence at all for K <= kTC.
+//  * Flavours: a replay phase (advance over the accepted prefix of a replay
+//    block, write h_j) and/or a verify phase (y for every draft token; the
+//    fused flavour writes h_j, j = accept_len, straight from registers).
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -51,9 +54,10 @@
 
 namespace {
 
-constexpr int kTC = 8;                              // draft tokens staged in shared memory at a time
+constexpr int kTC = 8;                              // draft tokens per chunk (one mma n-block)
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // give up on a bulk copy after 1 s
 constexpr uint32_t kWaitLimitIters = 1u << 26;      // ... or after this many polls, whichever first
+constexpr int kThreads = 128;                       // 4 warps per CTA
 
 enum Flavour : int {
     kVerify = 0,        // verify phase only; the state is read-only
@@ -69,31 +73,60 @@ struct Flav {
     static constexpr bool kWriteInVerify = F == kVerifyCommit;
 };
 
-// Per-N geometry: N/8 lanes per row group, 8 rows per thread.
+// Per-N geometry. A band is 16 rows (one mma M block); WPB warps share a
+// band by columns (2 at N = 256, else 1). A thread holds rows g and g + 8 of
+// its band and NC of the band's columns: the 4-column chunks tq, tq + 4,
+// tq + 8, ... (tq = lane % 4) of its warp's column range.
 template <int N>
 struct Geo {
-    static constexpr int kLanesPerGroup = N / 8;
-    static constexpr int kGroupsPerWarp = 32 / kLanesPerGroup;
-    static constexpr int kRowsPerWarp = kGroupsPerWarp * 8;
-    static constexpr int kRows = kRowsPerWarp > 64 ? kRowsPerWarp : 64;  // rows per tile
-    static constexpr int kWarps = kRows / kRowsPerWarp;
-    static constexpr int kThreads = kWarps * 32;
-    static constexpr int kMinBlocks = 512 / kThreads;  // 128 registers per thread at most
+    static constexpr int kWPB = N > 128 ? N / 128 : 1;   // warps per band
+    static constexpr int kNCW = N / kWPB;                // columns per warp
+    static constexpr int kNC = kNCW / 4;                 // columns per thread (and per row)
+    static constexpr int kKB = kNCW / 8;                 // mma k-blocks per warp
+    static constexpr int kBands = 4 / kWPB;
+    static constexpr int kRows = 16 * kBands;            // rows per tile
+    static constexpr int kPad = kNC + 4;                 // padded row of a thread's slots in smem
     static_assert(N >= 16 && N <= 256 && (N & (N - 1)) == 0, "dstate must be a power of two in [16, 256]");
 };
 
-// Dynamic shared memory layout (byte offsets). The state buffer comes first
-// (the bulk copy destination, 128-byte aligned).
-template <int N, bool WANT_Y>
-struct Smem {
-    static constexpr int kRows = Geo<N>::kRows;
-    static constexpr int kState = 0;                                    // float [kRows][N]
-    static constexpr int kB = kState + kRows * N * 4;                   // float [kTC][N]
-    static constexpr int kC = kB + kTC * N * 4;                         // float [kTC][N]     (y only)
-    static constexpr int kU = kC + (WANT_Y ? kTC * N * 4 : 0);           // float [kTC][kRows]
-    static constexpr int kDx = kU + kTC * kRows * 4;                    // float [kTC][kRows] (y only)
-    static constexpr int kAbar = kDx + (WANT_Y ? kTC * kRows * 4 : 0);   // float [kTC]
-    static constexpr int kBytes = kAbar + kTC * 4;
+// Dynamic shared memory layout of one flavour (byte offsets, every region a
+// multiple of 16 bytes). The state tile first (bulk copy destination). Two
+// raw buffers, used by alternate tiles: the first chunk's x / B / C rows of
+// each phase as stored in global memory (bulk-copy destinations), so that the
+// next tile's copies can be issued before this tile's rows are converted.
+// Staged areas (fp32, what the arithmetic reads): B and C with each thread's
+// slots contiguous ([token][warp column half][tq][kPad]), u = dt x and D x
+// per row, Abar, cs (cumulative dt) and w per token.
+template <typename Tin, int N, int F>
+struct Lay {
+    using G = Geo<N>;
+    static constexpr int ROWS = G::kRows;
+    static constexpr bool R = Flav<F>::kReplay;
+    static constexpr bool V = Flav<F>::kVerifyPhase;
+    static constexpr int E = (int)sizeof(Tin);
+    static constexpr int BC = kTC * G::kWPB * 4 * G::kPad * 4;        // one permuted B or C chunk
+    static constexpr int kState = 0;                                    // float [ROWS][N]
+    // one raw buffer (offsets within it)
+    static constexpr int oVx = 0;                                       // Tin [kTC][ROWS]
+    static constexpr int oVB = oVx + (V ? kTC * ROWS * E : 0);          // Tin [kTC][N]
+    static constexpr int oVC = oVB + (V ? kTC * N * E : 0);             // Tin [kTC][N]
+    static constexpr int oRx = oVC + (V ? kTC * N * E : 0);             // Tin [kTC][ROWS]
+    static constexpr int oRB = oRx + (R ? kTC * ROWS * E : 0);          // Tin [kTC][N]
+    static constexpr int kRawBytes = oRB + (R ? kTC * N * E : 0);
+    static constexpr int kRaw = kState + ROWS * N * 4;                  // 2 raw buffers
+    static constexpr int kVB = kRaw + 2 * kRawBytes;                    // float, permuted
+    static constexpr int kVC = kVB + (V ? BC : 0);                      // float, permuted
+    static constexpr int kVU = kVC + (V ? BC : 0);                      // float [kTC][ROWS]
+    static constexpr int kVDx = kVU + (V ? kTC * ROWS * 4 : 0);         // float [kTC][ROWS]
+    static constexpr int kVAbar = kVDx + (V ? kTC * ROWS * 4 : 0);      // float [kTC]
+    static constexpr int kVCs = kVAbar + (V ? kTC * 4 : 0);             // float [kTC]
+    static constexpr int kVW = kVCs + (V ? kTC * 4 : 0);                // float [kTC]
+    static constexpr int kXch = kVW + (V ? kTC * 4 : 0);                // float [bands][32][8] (N = 256)
+    static constexpr int kRB = kXch + (V && G::kWPB > 1 ? G::kBands * 32 * 8 * 4 : 0);  // float, permuted
+    static constexpr int kRU = kRB + (R ? BC : 0);                      // float [kTC][ROWS]
+    static constexpr int kRAbar = kRU + (R ? kTC * ROWS * 4 : 0);       // float [kTC]
+    static constexpr int kBytes = kRAbar + (R ? kTC * 4 : 0);
+    static_assert(kRawBytes % 16 == 0 && kRaw % 128 == 0, "bulk-copy destinations must be 16-byte aligned");
 };
 
 // One block of draft tokens and its inputs (layouts in ssmverify.h).
@@ -102,6 +135,7 @@ struct Block {
     int K;        // tokens in the block: the extent of the token dimension
     int vec_x;    // x rows may be read 8 elements at a time with 16-byte loads
     int vec_bc;   // B / C rows likewise
+    int tma;      // the first chunk's x / B / C rows may be bulk-copied (16-byte aligned rows)
 };
 
 struct Args {
@@ -116,6 +150,12 @@ struct Args {
     int H, P, G, ptiles;
     long long ntiles;
 };
+
+// The kernels' dynamic shared memory (laid out by Lay).
+extern __shared__ __align__(128) char ssm_smem[];
+
+template <typename T>
+__device__ __forceinline__ T *sm(int off) { return reinterpret_cast<T *>(ssm_smem + off); }
 
 // ----------------------------------------------------------------------------- PTX helpers
 
@@ -179,13 +219,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// tf32 high part of x (round to nearest, ties away), as the bit pattern mma reads.
+__device__ __forceinline__ uint32_t tf32_hi(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d += a (16x8, row) * b (8x8, col), tf32 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ----------------------------------------------------------------------------- loads
 
 __device__ __forceinline__ float ld1(const float *p) { return __ldg(p); }
 __device__ __forceinline__ float ld1(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
 
 // Eight consecutive input elements as loaded (bf16 stays packed until it is
-// widened, to keep register pressure low while the state tile is live).
+// widened, to keep register pressure low).
 template <typename Tin>
 struct Raw8;
 template <>
@@ -225,6 +282,15 @@ __device__ __forceinline__ void ld8(const __nv_bfloat16 *p, bool vec, int valid,
     }
 }
 
+// The same eight elements from shared memory (16-byte aligned).
+__device__ __forceinline__ void lds8(const float *p, Raw8<float> &r) {
+    r.a = reinterpret_cast<const float4 *>(p)[0];
+    r.b = reinterpret_cast<const float4 *>(p)[1];
+}
+__device__ __forceinline__ void lds8(const __nv_bfloat16 *p, Raw8<__nv_bfloat16> &r) {
+    r.a = *reinterpret_cast<const uint4 *>(p);
+}
+
 // bf16 is the upper half of an fp32: widening is a 16-bit shift.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -239,9 +305,8 @@ __device__ __forceinline__ void widen(const Raw8<__nv_bfloat16> &r, float (&v)[8
     v[4] = bf16_lo(r.a.z); v[5] = bf16_hi(r.a.z); v[6] = bf16_lo(r.a.w); v[7] = bf16_hi(r.a.w);
 }
 
-__device__ __forceinline__ void st8(float *s, const float (&v)[8]) {
-    reinterpret_cast<float4 *>(s)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4 *>(s)[1] = make_float4(v[4], v[5], v[6], v[7]);
+__device__ __forceinline__ void st4(float *s, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(s) = make_float4(a, b, c, d);
 }
 
 // ----------------------------------------------------------------------------- arithmetic (shared by all flavours)
@@ -250,38 +315,20 @@ __device__ __forceinline__ void st8(float *s, const float (&v)[8]) {
 __device__ __forceinline__ float ssm_decay(float dt, float A) { return expf(__fmul_rn(dt, A)); }
 __device__ __forceinline__ float ssm_input_scale(float dt, float x) { return __fmul_rn(dt, x); }
 
-// One state update of two adjacent columns: h <- Abar h + (u B), two roundings.
+// One state update of two adjacent slots: h <- Abar h + (u B), two roundings.
 __device__ __forceinline__ float2 ssm_update2(float2 h, float2 abar2, float2 u2, float2 b2) {
     return __ffma2_rn(abar2, h, __fmul2_rn(u2, b2));
 }
 
-// Keep half of v[0..M) chosen by `bit`, send the other half to the partner
-// lane `lane ^ off`, add what the partner sends: afterwards v[0..M/2) holds
-// the pair's sums for rows base + (bit ? M/2 : 0) + i.
-template <int M>
-__device__ __forceinline__ void halve(float *v, bool bit, int off) {
-#pragma unroll
-    for (int i = 0; i < M / 2; ++i) {
-        const float lo = v[i], hi = v[i + M / 2];
-        const float keep = bit ? hi : lo;
-        const float send = bit ? lo : hi;
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-}
-
-// Reduce 8 per-thread row partials over the LG lanes of a row group.
-// Returns in v[0..M) the full sums of local rows `base .. base+M-1` of the
-// thread's 8 rows, with M = max(8 / LG, 1); lanes l >= 8 of the group hold
-// duplicates.
-template <int LG>
-__device__ __forceinline__ int reduce_rows(float (&v)[8], int l) {
-    int base = 0;
-    if constexpr (LG >= 2) { const bool b = l & 1; halve<8>(v, b, 1); base += b ? 4 : 0; }
-    if constexpr (LG >= 4) { const bool b = l & 2; halve<4>(v, b, 2); base += b ? 2 : 0; }
-    if constexpr (LG >= 8) { const bool b = l & 4; halve<2>(v, b, 4); base += b ? 1 : 0; }
-    if constexpr (LG >= 16) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
-    if constexpr (LG >= 32) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
-    return base;
+// Staged position of state column n (within [0, N)): the permuted B / C
+// arrays keep each thread's slots contiguous. Column n belongs to warp
+// column half n / kNCW, to the thread with tq = (n / 4) % 4 of that half, at
+// slot 4 * ((n / 4) / 4) + n % 4.
+template <int N>
+__device__ __forceinline__ int perm_index(int n) {
+    using G = Geo<N>;
+    const int half = n / G::kNCW, n2 = n % G::kNCW, c = n2 / 4;
+    return (half * 4 + (c & 3)) * G::kPad + 4 * (c >> 2) + (n2 & 3);
 }
 
 // ----------------------------------------------------------------------------- tile context
@@ -294,10 +341,11 @@ struct Tile {
 
 __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, int N) {
     Tile T;
-    const int ptile = (int)(t % a.ptiles);
-    const long long bh = t / a.ptiles;
-    T.h = (int)(bh % a.H);
-    T.b = bh / a.H;
+    const uint32_t tt = (uint32_t)t;  // the host keeps the tile count below 2^31
+    const int ptile = (int)(tt % (uint32_t)a.ptiles);
+    const uint32_t bh = tt / (uint32_t)a.ptiles;
+    T.h = (int)(bh % (uint32_t)a.H);
+    T.b = (long long)(bh / (uint32_t)a.H);
     T.g = T.h / (a.H / a.G);
     T.row0 = ptile * kRows;
     T.rows = min(kRows, a.P - T.row0);
@@ -305,175 +353,299 @@ __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, in
     return T;
 }
 
-// Stage tokens [t0, t0 + tc) of `blk` for tile T into shared memory laid out
-// as Smem<N, SMEMY>; WANT_Y also stages C and D x (the verify phase).
-// Work items: an x item is 8 rows of one token (u = dt x and D x), a B/C item
-// 8 columns of one token. When every thread has at most one item of each kind
-// (dstate >= 64) all of its loads are issued before the first use.
-template <typename Tin, int N, bool SMEMY, bool WANT_Y>
+// Accepted prefix j of sequence b against a block of kref tokens: an
+// out-of-range value counts as 0 and is reported.
+__device__ __forceinline__ int accepted(const Args &a, long long b, int kref) {
+    if (a.accept_len == nullptr) return kref;
+    const int j = __ldg(a.accept_len + b);
+    if (j < 0 || j > kref) {
+        if (threadIdx.x == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_ACCEPT_LEN);
+        return 0;
+    }
+    return j;
+}
+
+// Staged chunk of one phase: where its arrays live in shared memory.
+struct StagedOffsets {
+    int B, C, U, Dx, Abar, Cs, W, Xch;  // C, Dx, Cs, W, Xch: verify phase only
+};
+
+// dt values one thread needs to stage a chunk: the token of its x item
+// (thread tid < kTC * ROWS / 8 handles rows 8 (tid % (ROWS / 8)) .. + 7 of token
+// tid / (ROWS / 8)) and, for warp 0, token tid (Abar, cumulative dt). Issued
+// early so that their latency hides behind the wait for the bulk copies.
+struct ChunkDt {
+    float x, tok;
+};
+
+template <typename Tin, int N>
+__device__ __forceinline__ ChunkDt load_chunk_dt(const Args &a, const Block &blk, const Tile &T, int t0, int tc) {
+    constexpr int XPT = Geo<N>::kRows / 8;
+    const Tin *dtp = static_cast<const Tin *>(blk.dt);
+    const int tid = threadIdx.x;
+    const long long bt0 = T.b * blk.K + t0;
+    ChunkDt d;
+    const int tx = tid / XPT;
+    d.x = (tid < kTC * XPT && tx < tc) ? ld1(dtp + (bt0 + tx) * a.H + T.h) : 0.f;
+    d.tok = tid < tc ? ld1(dtp + (bt0 + tid) * a.H + T.h) : 0.f;
+    return d;
+}
+
+// Convert one chunk of tc tokens into the staged fp32 arrays, from the raw
+// rows in shared memory (FROM_RAW: offsets rawX / rawB / rawC) or from global
+// memory. x items are 8 rows of one token (u = dt x and D x), B/C items 8
+// columns of one token. Tokens tc .. kTC-1 of u are zeroed (they meet zero
+// weights in the intra-chunk contraction and must not be NaN). Warp 0 also
+// forms Abar, cs_t = sum_{r<=t} dt_r and w_t = exp(A cs_t) (verify phase).
+template <typename Tin, int N, bool WANT_Y, bool FROM_RAW>
 __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, const Tile &T, int t0, int tc, float Ah,
-                                            float Dh, char *smem) {
-    static_assert(SMEMY || !WANT_Y, "y staging needs the y layout");
-    using S = Smem<N, SMEMY>;
+                                            float Dh, const StagedOffsets &so, int rawX, int rawB, int rawC,
+                                            const ChunkDt &dt) {
     constexpr int ROWS = Geo<N>::kRows;
-    constexpr int THREADS = Geo<N>::kThreads;
     constexpr int XPT = ROWS / 8;  // x items per token
     constexpr int BPT = N / 8;     // B/C items per token
-    float *sB = reinterpret_cast<float *>(smem + S::kB);
-    float *sC = reinterpret_cast<float *>(smem + S::kC);
-    float *sU = reinterpret_cast<float *>(smem + S::kU);
-    float *sDx = reinterpret_cast<float *>(smem + S::kDx);
-    float *sAbar = reinterpret_cast<float *>(smem + S::kAbar);
+    static_assert(kTC * XPT <= kThreads, "one x item per thread");
     const Tin *xp = static_cast<const Tin *>(blk.x);
     const Tin *Bp = static_cast<const Tin *>(blk.B);
     const Tin *Cp = static_cast<const Tin *>(blk.C);
-    const Tin *dtp = static_cast<const Tin *>(blk.dt);
     const int tid = threadIdx.x;
     const long long bt0 = T.b * blk.K + t0;  // (b, t0) in [batch][K]
-    const int nx = tc * XPT, nb = tc * BPT;
 
-    auto x_item_store = [&](int i, float dtv, const Raw8<Tin> &xr) {
-        const int t = i / XPT, r8 = i % XPT;
-        float xv[8], u[8];
-        widen(xr, xv);
+    // x item: u = dt x and D x for 8 rows of one token; zeros past tc.
+    if (tid < kTC * XPT) {
+        const int t = tid / XPT, r8 = tid % XPT;
+        float xv[8];
+        const float dtv = dt.x;
+        if (t < tc) {
+            Raw8<Tin> r;
+            const long long row = (bt0 + t) * a.H + T.h;
+            if (FROM_RAW) lds8(sm<const Tin>(rawX) + t * ROWS + 8 * r8, r);
+            else ld8(xp + row * a.P + T.row0 + 8 * r8, blk.vec_x, T.rows - 8 * r8, r);
+            widen(r, xv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] = ssm_input_scale(dtv, xv[e]);
-        st8(sU + t * ROWS + 8 * r8, u);
+            for (int e = 0; e < 8; ++e)
+                if (8 * r8 + e >= T.rows) xv[e] = 0.f;  // past the tile: never stored
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+        }
+        float *u = sm<float>(so.U) + t * ROWS + 8 * r8;
+        st4(u, ssm_input_scale(dtv, xv[0]), ssm_input_scale(dtv, xv[1]), ssm_input_scale(dtv, xv[2]),
+            ssm_input_scale(dtv, xv[3]));
+        st4(u + 4, ssm_input_scale(dtv, xv[4]), ssm_input_scale(dtv, xv[5]), ssm_input_scale(dtv, xv[6]),
+            ssm_input_scale(dtv, xv[7]));
         if (WANT_Y) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xv[e] = __fmul_rn(Dh, xv[e]);
-            st8(sDx + t * ROWS + 8 * r8, xv);
+            float *dx = sm<float>(so.Dx) + t * ROWS + 8 * r8;
+            st4(dx, __fmul_rn(Dh, xv[0]), __fmul_rn(Dh, xv[1]), __fmul_rn(Dh, xv[2]), __fmul_rn(Dh, xv[3]));
+            st4(dx + 4, __fmul_rn(Dh, xv[4]), __fmul_rn(Dh, xv[5]), __fmul_rn(Dh, xv[6]), __fmul_rn(Dh, xv[7]));
         }
-    };
-    auto x_item_load = [&](int i, float &dtv, Raw8<Tin> &xr) {
-        const int t = i / XPT, r8 = i % XPT;
-        const long long row = (bt0 + t) * a.H + T.h;
-        dtv = ld1(dtp + row);
-        ld8(xp + row * a.P + T.row0 + 8 * r8, blk.vec_x, T.rows - 8 * r8, xr);
-    };
-    auto bc_off = [&](int i) {
+    }
+    // B / C items: 8 columns = two 4-column chunks, each to its thread's slots.
+#pragma unroll 1
+    for (int i = tid; i < tc * BPT; i += kThreads) {
         const int t = i / BPT, n8 = i % BPT;
-        return ((bt0 + t) * a.G + T.g) * N + 8 * n8;
-    };
-    auto bc_store = [&](int i, float *dst, const Raw8<Tin> &r) {
-        const int t = i / BPT, n8 = i % BPT;
+        const long long off = ((bt0 + t) * a.G + T.g) * N + 8 * n8;
+        const int tb = t * Geo<N>::kWPB * 4 * Geo<N>::kPad;
+        const int p0 = tb + perm_index<N>(8 * n8), p1 = tb + perm_index<N>(8 * n8 + 4);
+        Raw8<Tin> r;
         float v[8];
+        if (FROM_RAW) lds8(sm<const Tin>(rawB) + t * N + 8 * n8, r);
+        else ld8(Bp + off, blk.vec_bc, 8, r);
         widen(r, v);
-        st8(dst + t * N + 8 * n8, v);
-    };
-
-    if constexpr (kTC * XPT <= THREADS && kTC * BPT <= THREADS) {
-        // One item of each kind per thread: issue every load, then convert.
-        const bool hx = tid < nx, hb = tid < nb;
-        float dtv = 0.f;
-        Raw8<Tin> xr, br, cr;
-        if (hx) x_item_load(tid, dtv, xr);
-        if (hb) {
-            ld8(Bp + bc_off(tid), blk.vec_bc, 8, br);
-            if (WANT_Y) ld8(Cp + bc_off(tid), blk.vec_bc, 8, cr);
+        st4(sm<float>(so.B) + p0, v[0], v[1], v[2], v[3]);
+        st4(sm<float>(so.B) + p1, v[4], v[5], v[6], v[7]);
+        if (WANT_Y) {
+            if (FROM_RAW) lds8(sm<const Tin>(rawC) + t * N + 8 * n8, r);
+            else ld8(Cp + off, blk.vec_bc, 8, r);
+            widen(r, v);
+            st4(sm<float>(so.C) + p0, v[0], v[1], v[2], v[3]);
+            st4(sm<float>(so.C) + p1, v[4], v[5], v[6], v[7]);
         }
-        if (tid < tc) sAbar[tid] = ssm_decay(ld1(dtp + (bt0 + tid) * a.H + T.h), Ah);
-        if (hx) x_item_store(tid, dtv, xr);
-        if (hb) {
-            bc_store(tid, sB, br);
-            if (WANT_Y) bc_store(tid, sC, cr);
-        }
-    } else {
-        if (tid < tc) sAbar[tid] = ssm_decay(ld1(dtp + (bt0 + tid) * a.H + T.h), Ah);
-#pragma unroll 1
-        for (int i = tid; i < nx; i += THREADS) {
-            float dtv;
-            Raw8<Tin> xr;
-            x_item_load(i, dtv, xr);
-            x_item_store(i, dtv, xr);
-        }
-#pragma unroll 1
-        for (int i = tid; i < nb; i += THREADS) {
-            Raw8<Tin> br, cr;
-            ld8(Bp + bc_off(i), blk.vec_bc, 8, br);
-            if (WANT_Y) ld8(Cp + bc_off(i), blk.vec_bc, 8, cr);
-            bc_store(i, sB, br);
-            if (WANT_Y) bc_store(i, sC, cr);
+    }
+    // Per token: Abar (and, for y, the cumulative dt and the decay w from the chunk start).
+    if (tid < 32) {
+        const float dtv = dt.tok;  // 0 for tid >= tc
+        if (tid < tc) sm<float>(so.Abar)[tid] = ssm_decay(dtv, Ah);
+        if (WANT_Y) {
+            float cs = dtv;  // inclusive prefix sum over the chunk's tokens
+#pragma unroll
+            for (int o = 1; o < kTC; o <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, cs, o);
+                if (tid >= o) cs += v;
+            }
+            if (tid < kTC) {
+                sm<float>(so.Cs)[tid] = cs;
+                sm<float>(so.W)[tid] = tid < tc ? expf(__fmul_rn(Ah, cs)) : 0.f;
+            }
         }
     }
 }
 
-// Store the thread's 8 rows of the state (rows at or past `valid` skipped).
+// Thread-local view: warp `wp` of the CTA, lane (g = lane / 4, tq = lane % 4).
+struct Lane {
+    int band, half, g, tq, lane;
+};
+
+// Load the thread's 2 x NC slots of the state tile from shared memory
+// (row-major [ROWS][N]); slots of rows past `rows` read as 0.
 template <int N>
-__device__ __forceinline__ void store_state(const float2 (&hs)[8][4], float *rows0, int c0, int c1, int valid) {
+__device__ __forceinline__ void load_state(float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L, int rows) {
+    using G = Geo<N>;
+    const float *sS = sm<const float>(0);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        if (r < valid) {
-            float *row = rows0 + r * N;
-            __stcs(reinterpret_cast<float4 *>(row + c0), make_float4(hs[r][0].x, hs[r][0].y, hs[r][1].x, hs[r][1].y));
-            __stcs(reinterpret_cast<float4 *>(row + c1), make_float4(hs[r][2].x, hs[r][2].y, hs[r][3].x, hs[r][3].y));
+    for (int rr = 0; rr < 2; ++rr) {
+        const int r = L.band * 16 + L.g + 8 * rr;
+        const float *row = sS + r * N + L.half * G::kNCW;
+#pragma unroll
+        for (int m = 0; m < G::kNC / 4; ++m) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < rows) v = *reinterpret_cast<const float4 *>(row + 4 * (L.tq + 4 * m));
+            hs[rr][2 * m] = make_float2(v.x, v.y);
+            hs[rr][2 * m + 1] = make_float2(v.z, v.w);
         }
     }
 }
 
-// Run `tc` staged tokens (layout Smem<N, SMEMY>) over the thread's state.
-// With WANT_Y, y of token t goes to ytok + t * ystride (rows relative to the
-// tile). With WRITE, the state after local token `wt` is stored to `srows`.
-template <int N, bool SMEMY, bool WANT_Y, bool WRITE>
-__device__ __forceinline__ void run_chunk(float2 (&hs)[8][4], const char *smem, int tc, int l, int rloc, int c0,
-                                          int c1, float *ytok, long long ystride, int tile_rows, int wt,
-                                          float *srows) {
-    static_assert(SMEMY || !WANT_Y, "y needs the y layout");
-    using S = Smem<N, SMEMY>;
-    constexpr int LG = Geo<N>::kLanesPerGroup;
-    constexpr int ROWS = Geo<N>::kRows;
-    constexpr int M = LG >= 8 ? 1 : 8 / LG;
-    const float *sB = reinterpret_cast<const float *>(smem + S::kB);
-    const float *sC = reinterpret_cast<const float *>(smem + S::kC);
-    const float *sU = reinterpret_cast<const float *>(smem + S::kU);
-    const float *sDx = reinterpret_cast<const float *>(smem + S::kDx);
-    const float *sAbar = reinterpret_cast<const float *>(smem + S::kAbar);
-
-    for (int t = 0; t < tc; ++t) {
-        // h_t = Abar_t h_{t-1} + u_t B_t^T for the thread's 64 elements.
-        const float abar = sAbar[t];
-        const float2 ab2 = make_float2(abar, abar);
-        const float4 b0 = *reinterpret_cast<const float4 *>(sB + t * N + c0);
-        const float4 b1 = *reinterpret_cast<const float4 *>(sB + t * N + c1);
-        const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                              make_float2(b1.z, b1.w)};
-        const float4 u0 = *reinterpret_cast<const float4 *>(sU + t * ROWS + rloc);
-        const float4 u1 = *reinterpret_cast<const float4 *>(sU + t * ROWS + rloc + 4);
-        const float ur[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+// Store the thread's slots of the state tile to global memory (rows past
+// `rows` skipped). `sl` = state + sbase + row0 * N.
+template <int N>
+__device__ __forceinline__ void store_state(const float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L, float *sl,
+                                            int rows) {
+    using G = Geo<N>;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float2 u2 = make_float2(ur[r], ur[r]);
+    for (int rr = 0; rr < 2; ++rr) {
+        const int r = L.band * 16 + L.g + 8 * rr;
+        if (r < rows) {
+            float *row = sl + (long long)r * N + L.half * G::kNCW;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) hs[r][k] = ssm_update2(hs[r][k], ab2, u2, bp[k]);
+            for (int m = 0; m < G::kNC / 4; ++m)
+                __stcs(reinterpret_cast<float4 *>(row + 4 * (L.tq + 4 * m)),
+                       make_float4(hs[rr][2 * m].x, hs[rr][2 * m].y, hs[rr][2 * m + 1].x, hs[rr][2 * m + 1].y));
         }
+    }
+}
 
-        if constexpr (WANT_Y) {
-            // y_t[p] = sum_n C_t[n] h_t[p][n] + D x_t[p].
-            const float4 q0 = *reinterpret_cast<const float4 *>(sC + t * N + c0);
-            const float4 q1 = *reinterpret_cast<const float4 *>(sC + t * N + c1);
-            const float2 cp[4] = {make_float2(q0.x, q0.y), make_float2(q0.z, q0.w), make_float2(q1.x, q1.y),
-                                  make_float2(q1.z, q1.w)};
-            float acc[8];
+// One recurrence step (staged token t): h <- Abar_t h + u_t[p] B_t^T.
+template <int N>
+__device__ __forceinline__ void recur_token(float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L, const StagedOffsets &so,
+                                            int t) {
+    using G = Geo<N>;
+    constexpr int ROWS = G::kRows;
+    const float abar = sm<const float>(so.Abar)[t];
+    const float2 ab2 = make_float2(abar, abar);
+    const float *urow = sm<const float>(so.U) + t * ROWS + L.band * 16 + L.g;
+    const float2 u0 = make_float2(urow[0], urow[0]);
+    const float2 u1 = make_float2(urow[8], urow[8]);
+    const float *bs = sm<const float>(so.B) + (t * G::kWPB * 4 + L.half * 4 + L.tq) * G::kPad;
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                float2 s = __fmul2_rn(cp[0], hs[r][0]);
-                s = __ffma2_rn(cp[1], hs[r][1], s);
-                s = __ffma2_rn(cp[2], hs[r][2], s);
-                s = __ffma2_rn(cp[3], hs[r][3], s);
-                acc[r] = s.x + s.y;
-            }
-            const int base = reduce_rows<LG>(acc, l);
-            if (l < 8) {
-                float *yt = ytok + t * ystride;
+    for (int m = 0; m < G::kNC / 4; ++m) {
+        const float4 b = *reinterpret_cast<const float4 *>(bs + 4 * m);
+        const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+        hs[0][2 * m] = ssm_update2(hs[0][2 * m], ab2, u0, b01);
+        hs[0][2 * m + 1] = ssm_update2(hs[0][2 * m + 1], ab2, u0, b23);
+        hs[1][2 * m] = ssm_update2(hs[1][2 * m], ab2, u1, b01);
+        hs[1][2 * m + 1] = ssm_update2(hs[1][2 * m + 1], ab2, u1, b23);
+    }
+}
+
+// The split of an fp32 operand for mma: exact inputs (bf16 values) need only
+// the high part.
+struct Split {
+    uint32_t hi, lo;
+};
+__device__ __forceinline__ Split split(float x) {
+    Split s;
+    s.hi = tf32_hi(x);
+    s.lo = __float_as_uint(x - __uint_as_float(s.hi));
+    return s;
+}
+
+// y for the staged verify chunk (tc tokens, chunk start state hs):
+//   y_t = w_t (C_t . h) + sum_{s<=t} L[t,s] (C_t . B_s) u_s + D x_t
+// h . C^T and C . B^T on the tensor cores; y stored to ychunk + t * ystride + row.
+template <typename Tin, int N>
+__device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L,
+                                        const StagedOffsets &so, int tc, float Ah, float *ychunk, long long ystride,
+                                        int rows) {
+    using G = Geo<N>;
+    constexpr int ROWS = G::kRows;
+    constexpr bool kExact = sizeof(Tin) == 2;  // bf16 B and C are exact tf32 values
+    const float *Cs = sm<const float>(so.C) + (L.g * G::kWPB * 4 + L.half * 4 + L.tq) * G::kPad;
+    const float *Bs = sm<const float>(so.B) + (L.g * G::kWPB * 4 + L.half * 4 + L.tq) * G::kPad;
+
+    // Y0 = h . C^T (rows g, g+8; tokens 2tq, 2tq+1) and Gm = C . B^T (row g = token t,
+    // columns 2tq, 2tq+1 = tokens s; rows g+8 of the mma are unused), over the warp's columns.
+    float y0[4] = {0.f, 0.f, 0.f, 0.f};
+    float gm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < M; ++i) {
-                    const int rl = rloc + base + i;
-                    if (rl < tile_rows) __stcs(yt + rl, acc[i] + sDx[t * ROWS + rl]);
-                }
-            }
+    for (int kb = 0; kb < G::kKB; ++kb) {
+        const float2 c = *reinterpret_cast<const float2 *>(Cs + 2 * kb);
+        const float2 bv = *reinterpret_cast<const float2 *>(Bs + 2 * kb);
+        const Split h00 = split(hs[0][kb].x), h10 = split(hs[1][kb].x), h01 = split(hs[0][kb].y),
+                    h11 = split(hs[1][kb].y);
+        if constexpr (kExact) {
+            const uint32_t c0 = __float_as_uint(c.x), c1 = __float_as_uint(c.y);
+            mma_tf32(y0, h00.lo, h10.lo, h01.lo, h11.lo, c0, c1);
+            mma_tf32(y0, h00.hi, h10.hi, h01.hi, h11.hi, c0, c1);
+            mma_tf32(gm, c0, 0u, c1, 0u, __float_as_uint(bv.x), __float_as_uint(bv.y));
+        } else {
+            const Split c0 = split(c.x), c1 = split(c.y), b0 = split(bv.x), b1 = split(bv.y);
+            mma_tf32(y0, h00.lo, h10.lo, h01.lo, h11.lo, c0.hi, c1.hi);
+            mma_tf32(y0, h00.hi, h10.hi, h01.hi, h11.hi, c0.lo, c1.lo);
+            mma_tf32(y0, h00.hi, h10.hi, h01.hi, h11.hi, c0.hi, c1.hi);
+            mma_tf32(gm, c0.lo, 0u, c1.lo, 0u, b0.hi, b1.hi);
+            mma_tf32(gm, c0.hi, 0u, c1.hi, 0u, b0.lo, b1.lo);
+            mma_tf32(gm, c0.hi, 0u, c1.hi, 0u, b0.hi, b1.hi);
         }
-
-        if (WRITE && t == wt) store_state<N>(hs, srows, c0, c1, tile_rows - rloc);
+    }
+    if constexpr (G::kWPB > 1) {
+        // The band's second column half hands its partial Y0 and Gm to the first
+        // through shared memory (a named barrier over the band's two warps).
+        float *x = sm<float>(so.Xch) + (L.band * 32 + L.lane) * 8;
+        if (L.half == 1) {
+            st4(x, y0[0], y0[1], y0[2], y0[3]);
+            x[4] = gm[0];
+            x[5] = gm[1];
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + L.band) : "memory");
+        if (L.half == 1) return;
+        y0[0] += x[0]; y0[1] += x[1]; y0[2] += x[2]; y0[3] += x[3];
+        gm[0] += x[4];
+        gm[1] += x[5];
+    }
+    // W[t][s] = L[t,s] Gm[t][s] for s <= t < tc (else 0); this lane holds t = g, s = 2tq, 2tq+1.
+    const float *cs = sm<const float>(so.Cs);
+    float w2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int t = L.g, s = 2 * L.tq + e;
+        w2[e] = (s <= t && t < tc) ? expf(__fmul_rn(Ah, cs[t] - cs[s])) * gm[e] : 0.f;
+    }
+    // The intra-chunk term U . W^T: B fragment b0 = W[g][tq], b1 = W[g][tq + 4],
+    // gathered from the quad holding row g.
+    const int src0 = (L.lane & ~3) | (L.tq >> 1), src1 = src0 + 2;
+    const float x0 = __shfl_sync(0xffffffffu, w2[0], src0), x1 = __shfl_sync(0xffffffffu, w2[1], src0);
+    const float z0 = __shfl_sync(0xffffffffu, w2[0], src1), z1 = __shfl_sync(0xffffffffu, w2[1], src1);
+    const Split wb0 = split((L.tq & 1) ? x1 : x0), wb1 = split((L.tq & 1) ? z1 : z0);
+    const float *U = sm<const float>(so.U) + L.band * 16 + L.g;
+    const Split ua0 = split(U[L.tq * ROWS]), ua1 = split(U[L.tq * ROWS + 8]), ua2 = split(U[(L.tq + 4) * ROWS]),
+                ua3 = split(U[(L.tq + 4) * ROWS + 8]);
+    // y = w (.) Y0 + U W^T
+    const float *wt = sm<const float>(so.W);
+    float d[4];
+    d[0] = y0[0] * wt[2 * L.tq];
+    d[1] = y0[1] * wt[2 * L.tq + 1];
+    d[2] = y0[2] * wt[2 * L.tq];
+    d[3] = y0[3] * wt[2 * L.tq + 1];
+    mma_tf32(d, ua0.lo, ua1.lo, ua2.lo, ua3.lo, wb0.hi, wb1.hi);
+    mma_tf32(d, ua0.hi, ua1.hi, ua2.hi, ua3.hi, wb0.lo, wb1.lo);
+    mma_tf32(d, ua0.hi, ua1.hi, ua2.hi, ua3.hi, wb0.hi, wb1.hi);
+    // + D x, store rows g, g + 8 for tokens 2tq, 2tq + 1.
+    const float *Dx = sm<const float>(so.Dx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = 2 * L.tq + (i & 1), r = L.band * 16 + L.g + 8 * (i >> 1);
+        if (t < tc && r < rows) __stcs(ychunk + t * ystride + r, d[i] + Dx[t * ROWS + r]);
     }
 }
 
@@ -495,120 +667,181 @@ __device__ __forceinline__ long long next_work(const Args &a, long long t) {
     }
 }
 
-// Register budget: 128 per thread (4 resident 128-thread CTAs at N = 128),
-// except commit_verify, whose two phases keep more addresses live next to the
-// state tile: 168 per thread (3 CTAs).
+#ifndef SSM_REGCAP
+#define SSM_REGCAP 128
+#endif
+// Register budget per thread (resident CTAs of 128 threads = 65536 / (128 x cap)).
 template <int N, int F>
 constexpr int min_blocks() {
-    return F == kCommitVerify ? (65536 / 168 / Geo<N>::kThreads > 0 ? 65536 / 168 / Geo<N>::kThreads : 1)
-                              : Geo<N>::kMinBlocks;
+    return 65536 / SSM_REGCAP / kThreads > 0 ? 65536 / SSM_REGCAP / kThreads : 1;
 }
 
 template <typename Tin, int N, int F>
-__global__ void __launch_bounds__(Geo<N>::kThreads, (min_blocks<N, F>())) ssm_tile_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kernel(const Args a) {
     using G = Geo<N>;
     using FL = Flav<F>;
-    constexpr int LG = G::kLanesPerGroup;
+    using LY = Lay<Tin, N, F>;
     constexpr int ROWS = G::kRows;
-    constexpr bool WANT_Y = FL::kVerifyPhase;
-    using S = Smem<N, WANT_Y>;
-
-    extern __shared__ __align__(128) char smem[];
+    constexpr int E = (int)sizeof(Tin);
     __shared__ uint64_t bar;
-    float *sS = reinterpret_cast<float *>(smem + S::kState);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int l = lane % LG;                                        // lane within the row group
-    const int rloc = (warp * G::kGroupsPerWarp + lane / LG) * 8;    // first local row of the thread
-    const int c0 = 4 * l, c1 = N / 2 + 4 * l;
+    Lane L;
+    L.band = warp / G::kWPB;
+    L.half = warp % G::kWPB;
+    L.g = lane >> 2;
+    L.tq = lane & 3;
+    L.lane = lane;
+    const StagedOffsets sV{LY::kVB, LY::kVC, LY::kVU, LY::kVDx, LY::kVAbar, LY::kVCs, LY::kVW, LY::kXch};
+    const StagedOffsets sR{LY::kRB, LY::kRB, LY::kRU, LY::kRU, LY::kRAbar, LY::kRAbar, LY::kRAbar, LY::kRAbar};
 
     long long t = next_work<F>(a, blockIdx.x);
     if (t >= a.ntiles) return;  // uniform over the CTA
 
-    auto prefetch = [&](long long tt) {
+    // Warp 0 streams a tile into shared memory: the state rows and, where the
+    // layout allows, the raw x / B / C rows of each phase's first chunk, all
+    // completing on `bar` as one transaction. plan() works out which copies
+    // lane `lane` issues (copy `lane` and copy `lane + 32` of the list
+    // [state, replay x rows, replay B rows, verify x rows, verify B rows,
+    // verify C rows]); issue() fires them.
+    struct Copy {
+        const void *src;
+        uint32_t dst, bytes;  // dst: offset into the dynamic shared memory; bytes 0: none
+    };
+    struct Plan {
+        Copy c[2];
+        uint32_t total;
+    };
+    auto plan = [&](long long tt, int buf) {
+        Plan pl;
+        pl.c[0].bytes = pl.c[1].bytes = 0;
+        pl.c[0].src = pl.c[1].src = nullptr;
+        pl.c[0].dst = pl.c[1].dst = 0;
+        pl.total = 0;
+        if (warp != 0 || tt >= a.ntiles) return pl;
         const Tile T = decode(a, tt, ROWS, N);
-        const uint32_t bytes = (uint32_t)T.rows * N * 4;
-        mbar_arrive_expect_tx(&bar, bytes);
-        bulk_load(sS, a.state_in + T.sbase + (long long)T.row0 * N, bytes, &bar);
+        const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.b, a.rep.K), kTC) : 0;
+        const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
+        const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
+        pl.total = (uint32_t)T.rows * N * 4 + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
+        const int ncopy = 1 + 2 * tcR + 3 * tcV;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = lane + 32 * q;
+            if (i >= ncopy) continue;
+            Copy &c = pl.c[q];
+            if (i == 0) {
+                c.src = a.state_in + T.sbase + (long long)T.row0 * N;
+                c.dst = LY::kState;
+                c.bytes = (uint32_t)T.rows * N * 4;
+                continue;
+            }
+            int k = i - 1;
+            const bool rep = k < 2 * tcR;
+            if (!rep) k -= 2 * tcR;
+            const int per = rep ? max(tcR, 1) : max(tcV, 1);
+            const int kind = k / per;  // 0: x row, 1: B row, 2: C row
+            const int tok = k % per;
+            const long long bt = T.b * (rep ? a.rep.K : a.ver.K) + tok;
+            if (kind == 0) {
+                c.src = static_cast<const Tin *>(rep ? a.rep.x : a.ver.x) + (bt * a.H + T.h) * a.P + T.row0;
+                c.dst = LY::kRaw + buf * LY::kRawBytes + (rep ? LY::oRx : LY::oVx) + tok * ROWS * E;
+                c.bytes = xrow;
+            } else {
+                const void *bc = rep ? a.rep.B : (kind == 1 ? a.ver.B : a.ver.C);
+                c.src = static_cast<const Tin *>(bc) + (bt * a.G + T.g) * N;
+                c.dst = LY::kRaw + buf * LY::kRawBytes + (rep ? LY::oRB : (kind == 1 ? LY::oVB : LY::oVC)) +
+                        tok * N * E;
+                c.bytes = bcrow;
+            }
+        }
+        return pl;
+    };
+    auto issue = [&](const Plan &pl) {
+        if (lane == 0) mbar_arrive_expect_tx(&bar, pl.total);
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (pl.c[q].bytes != 0) bulk_load(ssm_smem + pl.c[q].dst, pl.c[q].src, pl.c[q].bytes, &bar);
     };
 
     if (tid == 0) {
         mbar_init(&bar, 1);
         fence_barrier_init();
         fence_proxy_async_smem();
-        prefetch(t);
     }
     __syncthreads();
+    if (warp == 0) issue(plan(t, 0));
 
-    const float *Aall = a.A;
-    uint32_t parity = 0;
+    uint32_t parity = 0;  // mbarrier phase; raw buffer of the current tile = parity
     while (t < a.ntiles) {
         const Tile T = decode(a, t, ROWS, N);
-        const float Ah = __ldg(Aall + T.h);
-        const float Dh = WANT_Y ? __ldg(a.D + T.h) : 0.f;
-
-        // The tile's state: shared memory (filled by the bulk copy) -> registers.
-        const bool ok = mbar_wait_bounded(&bar, parity);
-        float2 hs[8][4];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float *row = sS + (rloc + r) * N;
-            float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
-            if (rloc + r < T.rows) {
-                v0 = *reinterpret_cast<const float4 *>(row + c0);
-                v1 = *reinterpret_cast<const float4 *>(row + c1);
-            }
-            hs[r][0] = make_float2(v0.x, v0.y);
-            hs[r][1] = make_float2(v0.z, v0.w);
-            hs[r][2] = make_float2(v1.x, v1.y);
-            hs[r][3] = make_float2(v1.z, v1.w);
-        }
+        const float Ah = __ldg(a.A + T.h);
+        const float Dh = FL::kVerifyPhase ? __ldg(a.D + T.h) : 0.f;
+        const int jr = FL::kReplay ? accepted(a, T.b, a.rep.K) : 0;             // tokens replayed
+        const int jw = FL::kWriteInVerify ? accepted(a, T.b, a.ver.K) - 1 : -1;  // verify token written after
+        const int tcR0 = min(jr, kTC), tcV0 = FL::kVerifyPhase ? min(a.ver.K, kTC) : 0;
         const long long tn = next_work<F>(a, t + gridDim.x);
-        // Every thread is done with the state buffer and with the previous
-        // tile's staged inputs; the vote makes a timeout a CTA-wide decision.
+        const Plan next = plan(tn, (int)(parity ^ 1u));
+        ChunkDt dR{0.f, 0.f}, dV{0.f, 0.f};
+        if constexpr (FL::kReplay) dR = load_chunk_dt<Tin, N>(a, a.rep, T, 0, tcR0);
+        if constexpr (FL::kVerifyPhase) dV = load_chunk_dt<Tin, N>(a, a.ver, T, 0, tcV0);
+
+        // Wait for the tile's bulk copies; the state tile goes to registers.
+        const bool ok = mbar_wait_bounded(&bar, parity);
+        float2 hs[2][G::kNC / 2];
+        load_state<N>(hs, L, T.rows);
+        // Every thread is done with the state tile and with the previous tile's
+        // staged inputs; the vote makes a timeout a CTA-wide decision.
         if (__syncthreads_or(!ok)) {
             if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
-            mbar_wait_bounded(&bar, parity);  // drain the copy still in flight, bounded
+            mbar_wait_bounded(&bar, parity);  // drain the copies still in flight, bounded
             return;
         }
-        if (tid == 0 && tn < a.ntiles) {
+        if (warp == 0 && tn < a.ntiles) {
             fence_proxy_async_smem();
-            prefetch(tn);
+            issue(next);
+        }
+        // Stage the first chunk of each phase: from this tile's raw buffer, or
+        // from global memory where the layout does not allow bulk copies.
+        const int raw = LY::kRaw + (int)parity * LY::kRawBytes;
+        if constexpr (FL::kReplay) {
+            if (jr > 0) {
+                if (a.rep.tma)
+                    stage_chunk<Tin, N, false, true>(a, a.rep, T, 0, tcR0, Ah, 0.f, sR, raw + LY::oRx, raw + LY::oRB,
+                                                     raw + LY::oRB, dR);
+                else
+                    stage_chunk<Tin, N, false, false>(a, a.rep, T, 0, tcR0, Ah, 0.f, sR, 0, 0, 0, dR);
+            }
+        }
+        if constexpr (FL::kVerifyPhase) {
+            if (a.ver.tma)
+                stage_chunk<Tin, N, true, true>(a, a.ver, T, 0, tcV0, Ah, Dh, sV, raw + LY::oVx, raw + LY::oVB,
+                                                raw + LY::oVC, dV);
+            else
+                stage_chunk<Tin, N, true, false>(a, a.ver, T, 0, tcV0, Ah, Dh, sV, 0, 0, 0, dV);
         }
         parity ^= 1u;
+        __syncthreads();  // staged inputs visible
 
-        float *srows = (a.state != nullptr) ? a.state + T.sbase + (long long)(T.row0 + rloc) * N : nullptr;
-
-        // Accepted prefix j of this tile's sequence.
-        int jr = 0;  // tokens replayed from the replay block
-        int jw = -1; // verify-phase token after which the state is written (-1: none)
-        if constexpr (FL::kReplay || FL::kWriteInVerify) {
-            const int kref = FL::kReplay ? a.rep.K : a.ver.K;
-            int j = kref;
-            if (a.accept_len != nullptr) {
-                j = __ldg(a.accept_len + T.b);
-                if (j < 0 || j > kref) {
-                    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_ACCEPT_LEN);
-                    j = 0;
-                }
-            }
-            if (FL::kReplay) jr = j;
-            else jw = j - 1;
-        }
+        float *sl = (a.state != nullptr) ? a.state + T.sbase + (long long)T.row0 * N : nullptr;
 
         if constexpr (FL::kReplay) {
             // Replay phase: advance over tokens 0 .. jr-1 of the replay block, then commit h_jr.
             for (int t0 = 0; t0 < jr; t0 += kTC) {
                 const int tc = min(kTC, jr - t0);
-                if (t0 > 0) __syncthreads();
-                stage_chunk<Tin, N, WANT_Y, false>(a, a.rep, T, t0, tc, Ah, 0.f, smem);
-                __syncthreads();
-                run_chunk<N, WANT_Y, false, false>(hs, smem, tc, l, rloc, c0, c1, nullptr, 0, T.rows, -1, nullptr);
+                if (t0 > 0) {
+                    const ChunkDt d = load_chunk_dt<Tin, N>(a, a.rep, T, t0, tc);
+                    __syncthreads();
+                    stage_chunk<Tin, N, false, false>(a, a.rep, T, t0, tc, Ah, 0.f, sR, 0, 0, 0, d);
+                    __syncthreads();
+                }
+#pragma unroll 1
+                for (int s = 0; s < tc; ++s) recur_token<N>(hs, L, sR, s);
             }
-            if (jr > 0) store_state<N>(hs, srows, c0, c1, T.rows - rloc);
-            if (FL::kVerifyPhase && jr > 0) __syncthreads();  // the verify phase restages the buffers
+            if (jr > 0) store_state<N>(hs, L, sl, T.rows);
         }
 
         if constexpr (FL::kVerifyPhase) {
@@ -617,11 +850,23 @@ __global__ void __launch_bounds__(Geo<N>::kThreads, (min_blocks<N, F>())) ssm_ti
             const long long ystride = (long long)a.H * a.P;
             for (int t0 = 0; t0 < K; t0 += kTC) {
                 const int tc = min(kTC, K - t0);
-                if (t0 > 0) __syncthreads();
-                stage_chunk<Tin, N, true, true>(a, a.ver, T, t0, tc, Ah, Dh, smem);
-                __syncthreads();
-                run_chunk<N, true, true, FL::kWriteInVerify>(hs, smem, tc, l, rloc, c0, c1, ytile + t0 * ystride,
-                                                       ystride, T.rows, jw - t0, srows);
+                if (t0 > 0) {
+                    const ChunkDt d = load_chunk_dt<Tin, N>(a, a.ver, T, t0, tc);
+                    __syncthreads();
+                    stage_chunk<Tin, N, true, false>(a, a.ver, T, t0, tc, Ah, Dh, sV, 0, 0, 0, d);
+                    __syncthreads();
+                }
+                chunk_y<Tin, N>(hs, L, sV, tc, Ah, ytile + t0 * ystride, ystride, T.rows);
+                // Advance the state by the recurrence as far as it is needed: through the
+                // chunk when more chunks follow, else up to the committed token.
+                int steps = 0;
+                if (t0 + tc < K) steps = tc;
+                else if (FL::kWriteInVerify && jw >= t0) steps = jw - t0 + 1;
+#pragma unroll 1
+                for (int s = 0; s < steps; ++s) {
+                    recur_token<N>(hs, L, sV, s);
+                    if (FL::kWriteInVerify && t0 + s == jw) store_state<N>(hs, L, sl, T.rows);
+                }
             }
         }
         t = tn;
@@ -675,8 +920,8 @@ constexpr int kMaxDevices = 64;
 
 template <typename Tin, int N, int F>
 cudaError_t launch_t(const Args &a, cudaStream_t s) {
-    constexpr int THREADS = Geo<N>::kThreads;
-    constexpr int SMEM = Smem<N, Flav<F>::kVerifyPhase>::kBytes;
+    constexpr int THREADS = kThreads;
+    constexpr int SMEM = Lay<Tin, N, F>::kBytes;
     static std::atomic<int> grid_cache[kMaxDevices];  // SMs x resident CTAs, 0 = unknown
     auto kern = ssm_tile_kernel<Tin, N, F>;
     int dev = 0;
@@ -767,6 +1012,7 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
     const int ROWS = rows_per_tile(N);
     const int64_t ptiles = (d->headdim + ROWS - 1) / ROWS;
     const int64_t ntiles = (int64_t)d->batch * d->nheads * ptiles;
+    if (ntiles >= (int64_t)1 << 31) return SSM_ERR_SHAPE;
     if (d->batch == 0) return SSM_OK;
 
     const void *st = F == kVerify ? static_cast<const void *>(c.state_in) : static_cast<const void *>(c.state);
@@ -826,6 +1072,7 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
     a.ver.K = d->ntok;
     a.ver.vec_x = verify_phase && aligned(c.x, 16) && rowb % 16 == 0;
     a.ver.vec_bc = verify_phase && aligned(c.B, 16) && aligned(c.C, 16);
+    a.ver.tma = a.ver.vec_x && a.ver.vec_bc;
     a.rep.x = c.xr;
     a.rep.B = c.Br;
     a.rep.C = nullptr;
@@ -833,6 +1080,7 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
     a.rep.K = rep_K;
     a.rep.vec_x = replay && aligned(c.xr, 16) && rowb % 16 == 0;
     a.rep.vec_bc = replay && aligned(c.Br, 16);
+    a.rep.tma = a.rep.vec_x && a.rep.vec_bc;
     a.A = c.A;
     a.D = c.D;
     a.accept_len = c.accept_len;
