@@ -372,8 +372,9 @@ struct StagedOffsets {
 
 // dt values one thread needs to stage a chunk: the token of its x item
 // (thread tid < kTC * ROWS / 8 handles rows 8 (tid % (ROWS / 8)) .. + 7 of token
-// tid / (ROWS / 8)) and, for warp 0, token tid (Abar, cumulative dt). Issued
-// early so that their latency hides behind the wait for the bulk copies.
+// tid / (ROWS / 8)) and, for lane l of the last warp, token l (Abar,
+// cumulative dt). Loaded one tile ahead so that their latency hides behind
+// the previous tile's work.
 struct ChunkDt {
     float x, tok;
 };
@@ -387,7 +388,8 @@ __device__ __forceinline__ ChunkDt load_chunk_dt(const Args &a, const Block &blk
     ChunkDt d;
     const int tx = tid / XPT;
     d.x = (tid < kTC * XPT && tx < tc) ? ld1(dtp + (bt0 + tx) * a.H + T.h) : 0.f;
-    d.tok = tid < tc ? ld1(dtp + (bt0 + tid) * a.H + T.h) : 0.f;
+    const int lt = tid - (kThreads - 32);  // token lane of the last warp
+    d.tok = (lt >= 0 && lt < tc) ? ld1(dtp + (bt0 + lt) * a.H + T.h) : 0.f;
     return d;
 }
 
@@ -462,20 +464,22 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
             st4(sm<float>(so.C) + p1, v[4], v[5], v[6], v[7]);
         }
     }
-    // Per token: Abar (and, for y, the cumulative dt and the decay w from the chunk start).
-    if (tid < 32) {
-        const float dtv = dt.tok;  // 0 for tid >= tc
-        if (tid < tc) sm<float>(so.Abar)[tid] = ssm_decay(dtv, Ah);
+    // Per token (the last warp, whose lanes carry no tile-copy work): Abar and,
+    // for y, the cumulative dt and the decay w from the chunk start.
+    const int lt = tid - (kThreads - 32);
+    if (lt >= 0) {
+        const float dtv = dt.tok;  // 0 for lt >= tc
+        if (lt < tc) sm<float>(so.Abar)[lt] = ssm_decay(dtv, Ah);
         if (WANT_Y) {
             float cs = dtv;  // inclusive prefix sum over the chunk's tokens
 #pragma unroll
             for (int o = 1; o < kTC; o <<= 1) {
                 const float v = __shfl_up_sync(0xffffffffu, cs, o);
-                if (tid >= o) cs += v;
+                if (lt >= o) cs += v;
             }
-            if (tid < kTC) {
-                sm<float>(so.Cs)[tid] = cs;
-                sm<float>(so.W)[tid] = tid < tc ? expf(__fmul_rn(Ah, cs)) : 0.f;
+            if (lt < kTC) {
+                sm<float>(so.Cs)[lt] = cs;
+                sm<float>(so.W)[lt] = lt < tc ? expf(__fmul_rn(Ah, cs)) : 0.f;
             }
         }
     }
@@ -487,21 +491,33 @@ struct Lane {
 };
 
 // Load the thread's 2 x NC slots of the state tile from shared memory
-// (row-major [ROWS][N]); slots of rows past `rows` read as 0.
+// (row-major [ROWS][N]); slots of rows past `rows` read as 0. Rows g and
+// g + 1 of a quarter warp sit on the same banks (rows are multiples of 128
+// bytes apart), so lanes with odd g fetch their column chunks in an order
+// rotated by one: the two rows' accesses land 16 banks apart and every
+// 128-bit load is conflict-free. The values are put back in slot order after.
 template <int N>
 __device__ __forceinline__ void load_state(float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L, int rows) {
     using G = Geo<N>;
+    constexpr int M = G::kNC / 4;  // 4-column chunks per thread and row
     const float *sS = sm<const float>(0);
+    const int rot = (M > 1) ? (L.g & 1) : 0;
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int r = L.band * 16 + L.g + 8 * rr;
         const float *row = sS + r * N + L.half * G::kNCW;
+        float4 v[M];
 #pragma unroll
-        for (int m = 0; m < G::kNC / 4; ++m) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < rows) v = *reinterpret_cast<const float4 *>(row + 4 * (L.tq + 4 * m));
-            hs[rr][2 * m] = make_float2(v.x, v.y);
-            hs[rr][2 * m + 1] = make_float2(v.z, v.w);
+        for (int m = 0; m < M; ++m) {
+            const int mm = (m + rot) & (M - 1);
+            v[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < rows) v[m] = *reinterpret_cast<const float4 *>(row + 4 * (L.tq + 4 * mm));
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const float4 w = rot ? v[(m + M - 1) & (M - 1)] : v[m];
+            hs[rr][2 * m] = make_float2(w.x, w.y);
+            hs[rr][2 * m + 1] = make_float2(w.z, w.w);
         }
     }
 }
@@ -575,6 +591,9 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
 
     // Y0 = h . C^T (rows g, g+8; tokens 2tq, 2tq+1) and Gm = C . B^T (row g = token t,
     // columns 2tq, 2tq+1 = tokens s; rows g+8 of the mma are unused), over the warp's columns.
+    // The low-part products accumulate separately from the high-part ones
+    // (two shorter mma dependency chains), then are added in a fixed order.
+    float yl[4] = {0.f, 0.f, 0.f, 0.f};
     float y0[4] = {0.f, 0.f, 0.f, 0.f};
     float gm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -590,14 +609,16 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
             mma_tf32(gm, c0, 0u, c1, 0u, __float_as_uint(bv.x), __float_as_uint(bv.y));
         } else {
             const Split c0 = split(c.x), c1 = split(c.y), b0 = split(bv.x), b1 = split(bv.y);
-            mma_tf32(y0, h00.lo, h10.lo, h01.lo, h11.lo, c0.hi, c1.hi);
-            mma_tf32(y0, h00.hi, h10.hi, h01.hi, h11.hi, c0.lo, c1.lo);
+            mma_tf32(yl, h00.lo, h10.lo, h01.lo, h11.lo, c0.hi, c1.hi);
+            mma_tf32(yl, h00.hi, h10.hi, h01.hi, h11.hi, c0.lo, c1.lo);
             mma_tf32(y0, h00.hi, h10.hi, h01.hi, h11.hi, c0.hi, c1.hi);
             mma_tf32(gm, c0.lo, 0u, c1.lo, 0u, b0.hi, b1.hi);
             mma_tf32(gm, c0.hi, 0u, c1.hi, 0u, b0.lo, b1.lo);
             mma_tf32(gm, c0.hi, 0u, c1.hi, 0u, b0.hi, b1.hi);
         }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y0[i] += yl[i];
     if constexpr (G::kWPB > 1) {
         // The band's second column half hands its partial Y0 and Gm to the first
         // through shared memory (a named barrier over the band's two warps).
@@ -700,71 +721,59 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
     long long t = next_work<F>(a, blockIdx.x);
     if (t >= a.ntiles) return;  // uniform over the CTA
 
-    // Warp 0 streams a tile into shared memory: the state rows and, where the
-    // layout allows, the raw x / B / C rows of each phase's first chunk, all
-    // completing on `bar` as one transaction. plan() works out which copies
-    // lane `lane` issues (copy `lane` and copy `lane + 32` of the list
-    // [state, replay x rows, replay B rows, verify x rows, verify B rows,
-    // verify C rows]); issue() fires them.
-    struct Copy {
+    // A tile streams into shared memory as one transaction on `bar`: the state
+    // rows and, where the layout allows, the raw x / B / C rows of each
+    // phase's first chunk. The copies [state, replay x rows, replay B rows,
+    // verify x rows, verify B rows, verify C rows] are spread over the warps
+    // (copy k to lane k / 4 of warp k % 4); plan() works out this lane's copy
+    // (while the state registers are free), issue() fires it, and lane 0 of
+    // warp 0 announces the transaction's total bytes (a completion may arrive
+    // before the announcement: the mbarrier's transaction count goes negative
+    // meanwhile, and the phase cannot complete before the announcement).
+    struct Plan {
         const void *src;
         uint32_t dst, bytes;  // dst: offset into the dynamic shared memory; bytes 0: none
-    };
-    struct Plan {
-        Copy c[2];
         uint32_t total;
     };
     auto plan = [&](long long tt, int buf) {
-        Plan pl;
-        pl.c[0].bytes = pl.c[1].bytes = 0;
-        pl.c[0].src = pl.c[1].src = nullptr;
-        pl.c[0].dst = pl.c[1].dst = 0;
-        pl.total = 0;
-        if (warp != 0 || tt >= a.ntiles) return pl;
+        Plan pl{nullptr, 0u, 0u, 0u};
+        if (tt >= a.ntiles) return pl;
         const Tile T = decode(a, tt, ROWS, N);
         const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.b, a.rep.K), kTC) : 0;
         const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
         const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
         pl.total = (uint32_t)T.rows * N * 4 + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
         const int ncopy = 1 + 2 * tcR + 3 * tcV;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int i = lane + 32 * q;
-            if (i >= ncopy) continue;
-            Copy &c = pl.c[q];
-            if (i == 0) {
-                c.src = a.state_in + T.sbase + (long long)T.row0 * N;
-                c.dst = LY::kState;
-                c.bytes = (uint32_t)T.rows * N * 4;
-                continue;
-            }
-            int k = i - 1;
-            const bool rep = k < 2 * tcR;
-            if (!rep) k -= 2 * tcR;
-            const int per = rep ? max(tcR, 1) : max(tcV, 1);
-            const int kind = k / per;  // 0: x row, 1: B row, 2: C row
-            const int tok = k % per;
-            const long long bt = T.b * (rep ? a.rep.K : a.ver.K) + tok;
-            if (kind == 0) {
-                c.src = static_cast<const Tin *>(rep ? a.rep.x : a.ver.x) + (bt * a.H + T.h) * a.P + T.row0;
-                c.dst = LY::kRaw + buf * LY::kRawBytes + (rep ? LY::oRx : LY::oVx) + tok * ROWS * E;
-                c.bytes = xrow;
-            } else {
-                const void *bc = rep ? a.rep.B : (kind == 1 ? a.ver.B : a.ver.C);
-                c.src = static_cast<const Tin *>(bc) + (bt * a.G + T.g) * N;
-                c.dst = LY::kRaw + buf * LY::kRawBytes + (rep ? LY::oRB : (kind == 1 ? LY::oVB : LY::oVC)) +
-                        tok * N * E;
-                c.bytes = bcrow;
-            }
+        const int i = warp + 4 * lane;
+        if (i >= ncopy) return pl;
+        if (i == 0) {
+            pl.src = a.state_in + T.sbase + (long long)T.row0 * N;
+            pl.dst = LY::kState;
+            pl.bytes = (uint32_t)T.rows * N * 4;
+            return pl;
+        }
+        int k = i - 1;
+        const bool rep = k < 2 * tcR;
+        if (!rep) k -= 2 * tcR;
+        const int per = rep ? max(tcR, 1) : max(tcV, 1);
+        const int kind = k / per;  // 0: x row, 1: B row, 2: C row
+        const int tok = k % per;
+        const long long bt = T.b * (rep ? a.rep.K : a.ver.K) + tok;
+        if (kind == 0) {
+            pl.src = static_cast<const Tin *>(rep ? a.rep.x : a.ver.x) + (bt * a.H + T.h) * a.P + T.row0;
+            pl.dst = LY::kRaw + buf * LY::kRawBytes + (rep ? LY::oRx : LY::oVx) + tok * ROWS * E;
+            pl.bytes = xrow;
+        } else {
+            const void *bc = rep ? a.rep.B : (kind == 1 ? a.ver.B : a.ver.C);
+            pl.src = static_cast<const Tin *>(bc) + (bt * a.G + T.g) * N;
+            pl.dst = LY::kRaw + buf * LY::kRawBytes + (rep ? LY::oRB : (kind == 1 ? LY::oVB : LY::oVC)) + tok * N * E;
+            pl.bytes = bcrow;
         }
         return pl;
     };
     auto issue = [&](const Plan &pl) {
-        if (lane == 0) mbar_arrive_expect_tx(&bar, pl.total);
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-            if (pl.c[q].bytes != 0) bulk_load(ssm_smem + pl.c[q].dst, pl.c[q].src, pl.c[q].bytes, &bar);
+        if (tid == 0) mbar_arrive_expect_tx(&bar, pl.total);
+        if (pl.bytes != 0) bulk_load(ssm_smem + pl.dst, pl.src, pl.bytes, &bar);
     };
 
     if (tid == 0) {
@@ -773,21 +782,39 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         fence_proxy_async_smem();
     }
     __syncthreads();
-    if (warp == 0) issue(plan(t, 0));
+    issue(plan(t, 0));
+
+    // Per-tile scalars and the dt values of the first chunks, loaded one tile
+    // ahead (their latency hides behind the previous tile's work).
+    struct TileIn {
+        float Ah, Dh;
+        int jr, jw;  // tokens replayed; verify token after which the state is written (-1: none)
+        ChunkDt dR, dV;
+    };
+    auto load_in = [&](long long tt) {
+        TileIn in{0.f, 0.f, 0, -1, {0.f, 0.f}, {0.f, 0.f}};
+        if (tt >= a.ntiles) return in;
+        const Tile T = decode(a, tt, ROWS, N);
+        in.Ah = __ldg(a.A + T.h);
+        if (FL::kVerifyPhase) in.Dh = __ldg(a.D + T.h);
+        if (FL::kReplay) in.jr = accepted(a, T.b, a.rep.K);
+        if (FL::kWriteInVerify) in.jw = accepted(a, T.b, a.ver.K) - 1;
+        if constexpr (FL::kReplay) in.dR = load_chunk_dt<Tin, N>(a, a.rep, T, 0, min(in.jr, kTC));
+        if constexpr (FL::kVerifyPhase) in.dV = load_chunk_dt<Tin, N>(a, a.ver, T, 0, min(a.ver.K, kTC));
+        return in;
+    };
+    TileIn cur = load_in(t);
 
     uint32_t parity = 0;  // mbarrier phase; raw buffer of the current tile = parity
     while (t < a.ntiles) {
         const Tile T = decode(a, t, ROWS, N);
-        const float Ah = __ldg(a.A + T.h);
-        const float Dh = FL::kVerifyPhase ? __ldg(a.D + T.h) : 0.f;
-        const int jr = FL::kReplay ? accepted(a, T.b, a.rep.K) : 0;             // tokens replayed
-        const int jw = FL::kWriteInVerify ? accepted(a, T.b, a.ver.K) - 1 : -1;  // verify token written after
+        const float Ah = cur.Ah, Dh = cur.Dh;
+        const int jr = cur.jr, jw = cur.jw;
         const int tcR0 = min(jr, kTC), tcV0 = FL::kVerifyPhase ? min(a.ver.K, kTC) : 0;
+        const ChunkDt dR = cur.dR, dV = cur.dV;
         const long long tn = next_work<F>(a, t + gridDim.x);
         const Plan next = plan(tn, (int)(parity ^ 1u));
-        ChunkDt dR{0.f, 0.f}, dV{0.f, 0.f};
-        if constexpr (FL::kReplay) dR = load_chunk_dt<Tin, N>(a, a.rep, T, 0, tcR0);
-        if constexpr (FL::kVerifyPhase) dV = load_chunk_dt<Tin, N>(a, a.ver, T, 0, tcV0);
+        cur = load_in(tn);
 
         // Wait for the tile's bulk copies; the state tile goes to registers.
         const bool ok = mbar_wait_bounded(&bar, parity);
@@ -800,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
             mbar_wait_bounded(&bar, parity);  // drain the copies still in flight, bounded
             return;
         }
-        if (warp == 0 && tn < a.ntiles) {
+        if (tn < a.ntiles) {
             fence_proxy_async_smem();
             issue(next);
         }
