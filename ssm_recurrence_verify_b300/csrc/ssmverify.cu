@@ -591,8 +591,8 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
 
     // Y0 = h . C^T (rows g, g+8; tokens 2tq, 2tq+1) and Gm = C . B^T (row g = token t,
     // columns 2tq, 2tq+1 = tokens s; rows g+8 of the mma are unused), over the warp's columns.
-    // The low-part products accumulate separately from the high-part ones
-    // (two shorter mma dependency chains), then are added in a fixed order.
+    // fp32 inputs: the two low-part products accumulate in yl, apart from the
+    // high-part one, and are added in a fixed order after the loop.
     float yl[4] = {0.f, 0.f, 0.f, 0.f};
     float y0[4] = {0.f, 0.f, 0.f, 0.f};
     float gm[4] = {0.f, 0.f, 0.f, 0.f};
