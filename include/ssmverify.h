@@ -164,6 +164,17 @@ int ssm_commit_verify(const ssm_desc_t *desc, float *state, int32_t prev_ntok, c
 int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B, const void *C,
              const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
 
+/*
+ * ssm_selftest_wait_timeout -- failure-detection self-test of the bounded
+ * waits the kernels use for their bulk copies (every such wait gives up after
+ * about one second and reports SSM_STATUS_TIMEOUT instead of hanging). It
+ * launches one warp that waits on a transaction that is announced but never
+ * delivered (no copy is issued), so the wait runs out: after about one second
+ * SSM_STATUS_TIMEOUT is OR-ed into *dev_status (required, 4-byte aligned
+ * device word). Nothing else is touched and the device stays usable.
+ */
+int ssm_selftest_wait_timeout(uint32_t *dev_status, void *stream);
+
 /* A static, human-readable string for an SSM_* return code. */
 const char *ssm_strerror(int code);
 

@@ -189,6 +189,17 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// The same, with the source lines marked first to be evicted from L2 (data read once).
+__device__ __forceinline__ void bulk_load_once(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -773,7 +784,10 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
     };
     auto issue = [&](const Plan &pl) {
         if (tid == 0) mbar_arrive_expect_tx(&bar, pl.total);
-        if (pl.bytes != 0) bulk_load(ssm_smem + pl.dst, pl.src, pl.bytes, &bar);
+        if (pl.bytes != 0) {
+            if (pl.dst == LY::kState) bulk_load_once(ssm_smem + pl.dst, pl.src, pl.bytes, &bar);
+            else bulk_load(ssm_smem + pl.dst, pl.src, pl.bytes, &bar);
+        }
     };
 
     if (tid == 0) {
@@ -898,6 +912,21 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         }
         t = tn;
     }
+}
+
+// Failure-detection self-test: one warp waits, with the bounded wait of the
+// tile kernel, on an mbarrier phase whose announced bytes never arrive (no copy
+// is issued), and reports the timeout. Nothing but *status is touched.
+__global__ void ssm_wait_timeout_kernel(uint32_t *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        mbar_arrive_expect_tx(&bar, 16u);
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(&bar, 0u);
+    if (__any_sync(0xffffffffu, !ok) && threadIdx.x == 0 && status != nullptr) atomicOr(status, SSM_STATUS_TIMEOUT);
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -1201,6 +1230,18 @@ int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B,
     c.A = A; c.D = D; c.y = y;
     c.dev_status = dev_status;
     return run(desc, c, stream);
+}
+
+int ssm_selftest_wait_timeout(uint32_t *dev_status, void *stream) {
+    if (dev_status == nullptr) return SSM_ERR_NULL;
+    if (!aligned(dev_status, 4)) return SSM_ERR_ALIGN;
+    ssm_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
 }
 
 const char *ssm_strerror(int code) {

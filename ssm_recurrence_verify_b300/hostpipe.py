@@ -1,0 +1,133 @@
+"""Host-buffer front end: verify + commit with the draft inputs in host memory.
+
+A serving loop whose draft-token inputs arrive in (pinned) host memory and
+whose y goes back to the host pays for two PCIe transfers per layer-call, each
+larger than the kernel's own time. ``HostPipeline`` hides them behind each
+other: the batch is cut into sequence chunks, and three CUDA streams run
+chunk c's host-to-device copy, chunk c-1's kernel and chunk c-2's copy of y
+back to the host at the same time, through a ring of device staging slots.
+Every sequence's state, inputs and outputs are contiguous slices of the batch
+dimension, so chunks need no gathering. A whole step (one or several layers)
+can be captured once into a CUDA graph, so that issuing it costs one graph
+launch instead of dozens of copy, event and kernel calls. The kernels are the
+library's (``ssm_verify_commit`` through the C ABI); this module only orders
+copies and launches.
+"""
+from __future__ import annotations
+
+from typing import List, Optional
+
+import torch
+
+from . import ssmverify as sv
+
+
+class HostPipeline:
+    """``verify_commit`` for one layer with host-resident x, B, C, dt,
+    accept_len and y, on a device-resident state updated in place.
+
+    ``state`` is the device state ``[batch][H][P][N]`` (float32); ``A``, ``D``
+    are device ``[H]`` float32. Inputs given to :meth:`run` are host tensors
+    with the layouts of ``ssmverify`` (pinned memory for asynchronous copies).
+    ``chunks`` sequence chunks are processed per call; ``slots`` device staging
+    slots rotate between them. ``streams`` (copy-in, kernel, copy-out) may be
+    shared by the pipelines of several layers; each pipeline orders only its
+    own slots.
+    """
+
+    def __init__(self, state: torch.Tensor, A: torch.Tensor, D: torch.Tensor, ntok: int, ngroups: int,
+                 in_dtype: torch.dtype = torch.bfloat16, chunks: int = 2, slots: int = 3, streams=None):
+        if not state.is_cuda:
+            raise ValueError("state must be a CUDA tensor")
+        self.state, self.A, self.D = state, A, D
+        self.dev = state.device
+        bsz, H, P, N = state.shape
+        self.bsz, self.H, self.P, self.N, self.K, self.G = bsz, H, P, N, ntok, ngroups
+        self.chunks = max(1, min(chunks, bsz))
+        self.bounds = [(bsz * i) // self.chunks for i in range(self.chunks + 1)]
+        cmax = max(self.bounds[i + 1] - self.bounds[i] for i in range(self.chunks))
+        self.nslots = max(1, slots)
+
+        def dev(*shape, dtype=in_dtype):
+            return torch.empty(shape, dtype=dtype, device=self.dev)
+
+        self.slot_x = [dev(cmax, ntok, H, P) for _ in range(self.nslots)]
+        self.slot_B = [dev(cmax, ntok, ngroups, N) for _ in range(self.nslots)]
+        self.slot_C = [dev(cmax, ntok, ngroups, N) for _ in range(self.nslots)]
+        self.slot_dt = [dev(cmax, ntok, H) for _ in range(self.nslots)]
+        self.slot_acc = [dev(cmax, dtype=torch.int32) for _ in range(self.nslots)]
+        self.slot_y = [dev(cmax, ntok, H, P, dtype=torch.float32) for _ in range(self.nslots)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        if streams is None:
+            streams = tuple(torch.cuda.Stream(device=self.dev) for _ in range(3))
+        self.s_in, self.s_k, self.s_out = streams
+        # slot free again once its y has been copied out
+        self.freed: List[Optional[torch.cuda.Event]] = [None] * self.nslots
+
+    def run(self, x: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dt: torch.Tensor, accept_len: torch.Tensor,
+            y: torch.Tensor) -> None:
+        """Enqueue one layer-call: copies in, fused verify + commit per chunk,
+        y copied out. Asynchronous; synchronise on :attr:`s_out` (or the
+        device) before reading ``y`` or :attr:`status`."""
+        for c in range(self.chunks):
+            lo, hi = self.bounds[c], self.bounds[c + 1]
+            n = hi - lo
+            if n == 0:
+                continue
+            k = c % self.nslots
+            with torch.cuda.stream(self.s_in):
+                if self.freed[k] is not None:
+                    self.s_in.wait_event(self.freed[k])
+                self.slot_x[k][:n].copy_(x[lo:hi], non_blocking=True)
+                self.slot_B[k][:n].copy_(B[lo:hi], non_blocking=True)
+                self.slot_C[k][:n].copy_(C[lo:hi], non_blocking=True)
+                self.slot_dt[k][:n].copy_(dt[lo:hi], non_blocking=True)
+                self.slot_acc[k][:n].copy_(accept_len[lo:hi], non_blocking=True)
+                arrived = torch.cuda.Event()
+                arrived.record(self.s_in)
+            with torch.cuda.stream(self.s_k):
+                self.s_k.wait_event(arrived)
+                sv.verify_commit(self.state[lo:hi], self.slot_x[k][:n], self.slot_B[k][:n], self.slot_C[k][:n],
+                                 self.slot_dt[k][:n], self.A, self.D, self.slot_acc[k][:n], y=self.slot_y[k][:n],
+                                 dev_status=self.status, stream=self.s_k)
+                done = torch.cuda.Event()
+                done.record(self.s_k)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(done)
+                y[lo:hi].copy_(self.slot_y[k][:n], non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(self.s_out)
+                self.freed[k] = freed
+
+
+def capture_step(pipelines, inputs, device=None) -> torch.cuda.CUDAGraph:
+    """Capture one step -- ``pipelines[i].run(*inputs[i])`` for every i -- into
+    a CUDA graph and return it. The host and device buffers are fixed: replay
+    the graph after writing the next step's inputs into the same pinned host
+    tensors. The pipelines' streams fork from the capturing stream and join
+    back into it, so one replay covers the whole step and replays on one
+    stream run one after another."""
+    device = pipelines[0].dev if device is None else device
+    streams = []
+    for p in pipelines:
+        for s in (p.s_in, p.s_k, p.s_out):
+            if all(s is not t for t in streams):
+                streams.append(s)
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=device)
+    for p in pipelines:
+        p.freed = [None] * p.nslots
+    with torch.cuda.graph(g, stream=cap):
+        fork = torch.cuda.Event()
+        fork.record(cap)
+        for s in streams:
+            s.wait_event(fork)
+        for p, args in zip(pipelines, inputs):
+            p.run(*args)
+        for s in streams:
+            e = torch.cuda.Event()
+            e.record(s)
+            cap.wait_event(e)
+    for p in pipelines:
+        p.freed = [None] * p.nslots
+    return g

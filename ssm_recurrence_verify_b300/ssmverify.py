@@ -32,8 +32,8 @@ SSM_ERR_CUDA = 6
 SSM_STATUS_BAD_ACCEPT_LEN = 1
 SSM_STATUS_TIMEOUT = 2
 
-EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step", "ssm_strerror",
-           "ssm_last_cuda_error", "ssm_version")
+EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
+           "ssm_selftest_wait_timeout", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
 
 
 class SsmDesc(ctypes.Structure):
@@ -67,8 +67,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_verify_commit.argtypes = [dp] + [vp] * 11
     lib.ssm_commit_verify.argtypes = [dp, vp, ctypes.c_int32] + [vp] * 13
     lib.ssm_step.argtypes = [dp] + [vp] * 10
+    lib.ssm_selftest_wait_timeout.argtypes = [vp, vp]
     for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
-              "ssm_last_cuda_error", "ssm_version"):
+              "ssm_selftest_wait_timeout", "ssm_last_cuda_error", "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
     lib.ssm_strerror.restype = ctypes.c_char_p
@@ -204,6 +205,14 @@ def commit_verify(state, x_prev, B_prev, dt_prev, accept_len_prev, x, B, C, dt, 
                                             _ptr(dt_prev), _ptr(accept_len_prev), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
                                             _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
+
+
+def selftest_wait_timeout(dev_status, stream=None) -> None:
+    """Launch the bounded-wait self-test: after about one second the device
+    ORs SSM_STATUS_TIMEOUT into `dev_status` (int32 CUDA tensor, one word)."""
+    if not (dev_status.is_cuda and dev_status.dtype == torch.int32 and dev_status.numel() >= 1):
+        raise ValueError("dev_status must be an int32 CUDA tensor")
+    _check(load_library().ssm_selftest_wait_timeout(_ptr(dev_status), _stream(stream)))
 
 
 def step(state, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:

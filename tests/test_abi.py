@@ -232,3 +232,9 @@ def test_commit_verify_validation(lib):
     q = list(p)
     q[5] = q[1]                                           # the two blocks may share read-only buffers
     assert cv(lib, d, 3, q) == sv.SSM_ERR_CUDA
+
+
+@no_gpu_only
+def test_selftest_validation(lib):
+    assert lib.ssm_selftest_wait_timeout(None, None) == sv.SSM_ERR_NULL
+    assert lib.ssm_selftest_wait_timeout(ctypes.c_void_p(BASE + 2), None) == sv.SSM_ERR_ALIGN

@@ -42,3 +42,22 @@ def test_sentinels_untouched(cuda_device, shape):
     assert _intact(sbuf, s.numel())
     assert _intact(ybuf, y.numel())
     assert torch.isfinite(y).all() and torch.isfinite(s).all()
+
+
+def test_bounded_wait_times_out_and_device_stays_usable(cuda_device):
+    """The bounded wait gives up on a transaction that never completes,
+    reports SSM_STATUS_TIMEOUT, and the context keeps working afterwards."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    t0 = time.perf_counter()
+    ssm.ssmverify.selftest_wait_timeout(status)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(status.item()) == ssm.ssmverify.SSM_STATUS_TIMEOUT
+    assert 0.5 < waited < 30.0, waited
+    wl = synth.custom_workload(2, 2, 20, 16, 1, 3, synth.F32, seed=43)
+    d = to_dev(synth.draw_layer_round(wl), cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    y = ssm.verify_commit(d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], d["accept_len"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.isfinite(y).all()

@@ -1,0 +1,71 @@
+"""The host-buffer front end gives bitwise the results of the device-side
+verify_commit: y in host memory and the state updated in place, over several
+rounds and with chunk counts that do not divide the batch."""
+import pytest
+import torch
+
+import ssm_recurrence_verify_b300 as ssm
+from gpu_helpers import to_dev
+from ssm_recurrence_verify_b300 import synth
+from ssm_recurrence_verify_b300.hostpipe import HostPipeline
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("chunks,slots", [(1, 1), (3, 2), (5, 3)])
+def test_pipeline_equals_device_calls(cuda_device, chunks, slots):
+    wl = synth.custom_workload(11, 8, 64, 128, 2, 6, synth.BF16, seed=91)
+    p = synth.draw_params(wl)
+    st_ref = p["state0"].to(cuda_device)
+    st = st_ref.clone()
+    A, D = p["A"].to(cuda_device), p["D"].to(cuda_device)
+    pipe = HostPipeline(st, A, D, wl.ntok, wl.ngroups, torch.bfloat16, chunks=chunks, slots=slots)
+    for rnd in range(4):
+        t = synth.draw_tokens(wl, rnd)
+        acc = synth.draw_accept_len(wl, rnd)
+        td = to_dev(t, cuda_device)
+        y_ref = ssm.verify_commit(st_ref, td["x"], td["B"], td["C"], td["dt"], A, D, acc.to(cuda_device))
+        h = {k: v.pin_memory() for k, v in t.items()}
+        y = torch.full((wl.batch, wl.ntok, wl.nheads, wl.headdim), float("nan")).pin_memory()
+        pipe.run(h["x"], h["B"], h["C"], h["dt"], acc.pin_memory(), y)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref.cpu()), rnd
+        assert torch.equal(st, st_ref), rnd
+    assert int(pipe.status.item()) == 0
+
+
+def test_captured_step_equals_device_calls(cuda_device):
+    """Two layers' pipelines captured as one graph; three replays with new
+    inputs written into the same pinned buffers each time."""
+    from ssm_recurrence_verify_b300.hostpipe import capture_step
+    wl = synth.custom_workload(9, 4, 64, 64, 2, 5, synth.BF16, seed=92)
+    streams = tuple(torch.cuda.Stream(device=cuda_device) for _ in range(3))
+    refs, pipes, bufs = [], [], []
+    for layer in range(2):
+        p = synth.draw_params(wl, layer)
+        A, D = p["A"].to(cuda_device), p["D"].to(cuda_device)
+        st = p["state0"].to(cuda_device)
+        refs.append((st.clone(), A, D))
+        pipes.append(HostPipeline(st, A, D, wl.ntok, wl.ngroups, torch.bfloat16, chunks=4, slots=2,
+                                  streams=streams))
+        t = synth.draw_tokens(wl, 0, layer)
+        h = {k: v.pin_memory() for k, v in t.items()}
+        h["accept_len"] = synth.draw_accept_len(wl, 0).pin_memory()
+        h["y"] = torch.zeros((wl.batch, wl.ntok, wl.nheads, wl.headdim)).pin_memory()
+        bufs.append(h)
+    g = capture_step(pipes, [(h["x"], h["B"], h["C"], h["dt"], h["accept_len"], h["y"]) for h in bufs])
+    for rnd in range(1, 4):
+        for layer, h in enumerate(bufs):
+            t = synth.draw_tokens(wl, rnd, layer)
+            for k in ("x", "B", "C", "dt"):
+                h[k].copy_(t[k])
+            h["accept_len"].copy_(synth.draw_accept_len(wl, rnd))
+        g.replay()
+        torch.cuda.synchronize()
+        for layer, h in enumerate(bufs):
+            st_ref, A, D = refs[layer]
+            td = to_dev({k: h[k] for k in ("x", "B", "C", "dt", "accept_len")}, cuda_device)
+            y_ref = ssm.verify_commit(st_ref, td["x"], td["B"], td["C"], td["dt"], A, D, td["accept_len"])
+            torch.cuda.synchronize()
+            assert torch.equal(h["y"], y_ref.cpu()), (rnd, layer)
+            assert torch.equal(pipes[layer].state, st_ref), (rnd, layer)
