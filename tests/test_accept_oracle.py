@@ -77,8 +77,9 @@ def test_sample_equal_distributions_accept_everything():
     r = acc.accept_sample(tl, ql, drafts, u)
     assert r["accept_len"].tolist() == [K, K]
     for b in range(2):
-        c = np.cumsum(acc.softmax_f32(tl[b, K]), dtype=np.float32)
-        assert r["next_token"][b] == int(np.searchsorted(c, u[b, K] * c[-1], side="right"))
+        c = np.cumsum(acc.softmax_f32(tl[b, K]).astype(np.float64))
+        assert r["next_token"][b] == int(np.searchsorted(c, float(u[b, K]) * c[-1], side="right"))
+        assert r["next_lo"][b] == r["next_token"][b] == r["next_hi"][b]  # 7 well-separated weights
 
 
 def test_sample_rejects_tokens_the_verifier_rules_out():
@@ -198,3 +199,38 @@ def test_planted_sampling_mistakes_are_caught(kind):
 def test_pins_pass_on_the_committed_oracle():
     pin_hand_two_token(acc.accept_sample)
     pin_distribution(acc.accept_sample)
+
+
+# --------------------------------------------------------------------------- precision reporting
+
+def test_inverse_cdf_hand_values_and_admissible_range():
+    """Weights (1, 2, 3, 4), cumulative (1, 3, 6, 10). u = 0.5 puts the
+    threshold at 5: index 2 is the first with C > 5. With a band of 1.5,
+    lo = first C > 3.5 = index 2 and hi = first C > 6.5 = index 3."""
+    w = np.array([1, 2, 3, 4], dtype=np.float32)
+    assert acc.inverse_cdf(w, 0.5, 0.0) == (2, 2, 2)
+    assert acc.inverse_cdf(w, 0.5, 1.5) == (2, 2, 3)
+    assert acc.inverse_cdf(w, 0.0, 0.0) == (0, 0, 0)
+    # zero weights are never chosen: the threshold sits on a flat stretch
+    w = np.array([0, 1, 0, 0, 1, 0], dtype=np.float32)
+    assert acc.inverse_cdf(w, 0.5, 0.0)[0] == 4
+    assert acc.inverse_cdf(w, 0.25, 0.0)[0] == 1
+    # a threshold at the very top (rounding) falls back to the last positive weight
+    assert acc.inverse_cdf(w, 1.0, 0.0)[0] == 4
+    # nothing positive: the last index
+    assert acc.inverse_cdf(np.zeros(5, np.float32), 0.3, 0.0)[0] == 4
+
+
+def test_softmax_flushes_subnormal_exponentials():
+    row = np.array([0.0, -100.0, -80.0], dtype=np.float32)
+    p = acc.softmax_f32(row)
+    assert p[1] == 0.0                       # exp(-100) = 3.7e-44 is subnormal in fp32
+    assert p[2] == np.float32(np.exp(np.float32(-80.0)) / (1 + np.exp(np.float32(-80.0))))
+
+
+def test_near_accept_flags_only_close_calls():
+    p, q = [0.75, 0.25], [0.5, 0.5]          # draft token 1: ratio exactly 0.5
+    r = _sample([p, p], [q], [1], [0.5 + 1e-6, 0.3])
+    assert bool(r["near_accept"][0])
+    r = _sample([p, p], [q], [1], [0.49, 0.3])
+    assert not bool(r["near_accept"][0]) and r["accept_len"].tolist() == [1]
