@@ -209,9 +209,18 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+HOST_MARKER = "// ----------------------------------------------------------------------------- host side"
+
+
+def kernel_source_hash(path: str = KERNEL_SRC) -> str:
+    """sha256 of the device code of a kernel source: the text before its
+    host-side section, with #include lines left out, so that host-only edits
+    keep a recorded capture valid while any kernel edit voids it."""
+    with open(path) as f:
+        text = f.read()
+    dev = text.split(HOST_MARKER)[0]
+    dev = "\n".join(line for line in dev.splitlines() if not line.startswith("#include"))
+    return hashlib.sha256(dev.encode()).hexdigest()
 
 
 def recorded_traffic(workload_name: str):
@@ -392,6 +401,136 @@ def run_e2e(ssm, args, wl, s, stream, dev, world):
                     f"overlapped, one CUDA graph per step"}
 
 
+# ----------------------------------------------------------------------------- acceptance step
+
+ACCEPT_METRIC = "draft tokens decided/s (acceptance step); achieved HBM GB/s vs B300 peak"
+
+
+def accept_algorithmic_bytes(aw, batch: int, sample: bool) -> int:
+    """Bytes the acceptance step must move: every logit once, the draft
+    tokens (and uniforms), accept_len and next_token."""
+    K, V, es = aw.ntok, aw.vocab, aw.logit_bytes()
+    n = batch * (K + 1) * V * es + batch * K * 4 + batch * 8
+    if sample:
+        n += batch * K * V * es + batch * (K + 1) * 4
+    return n
+
+
+def run_accept(args, sample: bool, rank, world, local_rank):
+    """Time the device acceptance step (one launch per step) on the batched
+    serving workload's logits, with the same graph capture, L2 rotation and
+    clock sampling as the main path."""
+    import ssm_recurrence_verify_b300 as ssm
+    from ssm_recurrence_verify_b300 import build as libbuild
+    if not os.path.exists(libbuild.LIB):
+        libbuild.build()
+    ssm.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    aw = synth.ACCEPT_WORKLOADS[1]
+    batch, offset = shard(aw.batch, rank)
+    set_bytes = accept_algorithmic_bytes(aw, batch, sample)
+    nsets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
+    sets = []
+    for i in range(nsets):
+        w = synth.custom_accept_workload(aw.batch, aw.ntok, aw.vocab, aw.logit_dtype, seed=aw.seed + 1000 * i)
+        d = synth.draw_accept_inputs(w, batch=batch, batch_offset=offset)
+        e = {k: v.to(dev) for k, v in d.items()}
+        e["accept_len"] = torch.empty(batch, dtype=torch.int32, device=dev)
+        e["next_token"] = torch.empty(batch, dtype=torch.int32, device=dev)
+        e["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+        sets.append(e)
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(e):
+        if sample:
+            ssm.accept_sample(e["target_logits"], e["draft_logits"], e["draft_tokens"], e["uniform"],
+                              accept_len=e["accept_len"], next_token=e["next_token"], dev_status=e["status"],
+                              stream=stream)
+        else:
+            ssm.accept_greedy(e["target_logits"], e["draft_tokens"], accept_len=e["accept_len"],
+                              next_token=e["next_token"], dev_status=e["status"], stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for e in sets:
+            launch(e)
+    torch.cuda.synchronize()
+
+    def capture(idx):
+        out = []
+        for i in range(0, len(idx), MAX_GRAPH_LAUNCHES):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for si in idx[i:i + MAX_GRAPH_LAUNCHES]:
+                    launch(sets[si])
+            out.append(g)
+        return out
+
+    K = args.steps
+    warm = capture([i % nsets for i in range(args.warmup)])
+    timed = capture([(args.warmup + i) % nsets for i in range(K)])
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for g in warm:
+            g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for g in timed:
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    barrier(world)
+    sampler.stop()
+    for e in sets:
+        assert int(e["status"].item()) == 0, "device reported a bad draft token"
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    launch_ms = t0.elapsed_time(t1) / K
+    achieved = set_bytes / (launch_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    value = batch * world * aw.ntok * K / (ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import accept as acc
+        n_seq = 4
+        d = synth.draw_accept_inputs(aw, batch=n_seq)
+        reps, c0 = 0, time.perf_counter()
+        while True:
+            if sample:
+                acc.accept_sample(d["target_logits"], d["draft_logits"], d["draft_tokens"], d["uniform"])
+            else:
+                acc.accept_greedy(d["target_logits"], d["draft_tokens"])
+            reps += 1
+            if time.perf_counter() - c0 >= args.cpu_seconds:
+                break
+        el = time.perf_counter() - c0
+        cpu = {"value": n_seq * aw.ntok * reps / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_seq} of the {aw.batch} sequences, {reps} passes, {el:.1f} s, numpy single thread"}
+    rule = "speculative sampling" if sample else "greedy"
+    return {
+        "metric": ACCEPT_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": aw.name, "rule": rule, "batch_per_gpu": batch, "draft_tokens": aw.ntok,
+                   "vocab": aw.vocab, "logit_dtype": aw.logit_dtype,
+                   "l2": f"{nsets} independent input sets rotated ({set_bytes / 1e6:.0f} MB each)",
+                   "timing": f"timed steps captured as CUDA graphs of up to {MAX_GRAPH_LAUNCHES} launches"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": set_bytes, "launch_us_mean": launch_ms * 1e3},
+        "cpu_baseline": cpu, "gpu_launches": K, "clocks": sampler.summary(wall0, wall1),
+    }
+
+
 # ----------------------------------------------------------------------------- oracle (CPU) legs
 
 def oracle_throughput(wl, seconds: float, max_seqs: int = None):
@@ -494,6 +633,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy"], default="ssm",
+                    help="ssm: the verify/commit step (default); accept_*: the acceptance step alone")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -506,6 +647,14 @@ def main(argv=None):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.path != "ssm":
+        line = run_accept(args, args.path == "accept_sample", rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
     r = run_ours(args, wl, rank, world, local_rank)
 
     cpu = None

@@ -92,6 +92,7 @@ extern "C" {
 /* bits OR-ed into *dev_status by the device */
 #define SSM_STATUS_BAD_ACCEPT_LEN 1u
 #define SSM_STATUS_TIMEOUT 2u
+#define SSM_STATUS_BAD_TOKEN 4u /* acceptance: a draft token outside [0, vocab) */
 
 typedef struct {
     int32_t batch;    /* sequences */
@@ -174,6 +175,79 @@ int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B,
  * device word). Nothing else is touched and the device stays usable.
  */
 int ssm_selftest_wait_timeout(uint32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Acceptance of draft tokens (the step right after the verifier's pass).
+ *
+ * Source: the speculative-decoding section of the news summary (the draft
+ * proposes K tokens; tokens the verifier agrees with are accepted; at the
+ * first it does not, the remaining drafts are dropped and the state rolls
+ * back to the last accepted token; with all K accepted the next round
+ * starts) and the method overview of "The Mamba in the Llama", which calls
+ * the procedure a speculative sampling algorithm. accept_len is written to
+ * device memory in the layout ssm_commit / ssm_verify_commit /
+ * ssm_commit_verify read, so acceptance needs no trip through the host.
+ *
+ * Layouts (row-major, contiguous):
+ *   target_logits  logit_t [batch][ntok + 1][vocab]  verifier logits at every
+ *                  draft position and at the bonus position ntok
+ *   draft_logits   logit_t [batch][ntok][vocab]      draft-model logits
+ *   draft_tokens   int32   [batch][ntok]
+ *   uniform        float   [batch][ntok + 1]          U[0, 1) draws (sampling)
+ *   accept_len     int32   [batch]   out: j in [0, ntok]
+ *   next_token     int32   [batch]   out: the token that follows the accepted
+ *                  prefix (a correction after a rejection, the bonus token
+ *                  when j = ntok)
+ * logit_t is float (SSM_F32) or bf16 (SSM_BF16). Every row must hold at least
+ * one finite logit; NaN logits give unspecified results.
+ *
+ * Precision: probabilities are fp32 (exp(l - max) with subnormal results
+ * flushed to zero, divided by the row's sum). Sums run in an order of the
+ * library's choosing, so a decision whose threshold lies within fp32 rounding
+ * of the drawn uniform may go either way; the bound is about 3e-5 relative
+ * for an acceptance ratio and about 3e-5 of the summed probability mass for
+ * the next-token threshold.
+ *
+ * Alignment: logits their element size (16-byte aligned logits with
+ * vocab * element size a multiple of 16 take 128-bit loads; others a scalar
+ * path with the same results); the int32 / float arrays and dev_status 4
+ * bytes. Outputs must not overlap inputs or each other. A draft token outside
+ * [0, vocab) counts as a rejection at its position (the next token is then
+ * drawn from, or is the most likely token of, the verifier's distribution
+ * there) and ORs SSM_STATUS_BAD_TOKEN into *dev_status.
+ * ------------------------------------------------------------------------ */
+
+#define SSM_ACCEPT_MAX_NTOK 32
+#define SSM_ACCEPT_MAX_VOCAB (1 << 28)
+
+typedef struct {
+    int32_t batch;       /* sequences (0 is a no-op) */
+    int32_t ntok;        /* K: draft tokens per sequence, 1 .. SSM_ACCEPT_MAX_NTOK */
+    int32_t vocab;       /* V: 1 .. SSM_ACCEPT_MAX_VOCAB */
+    int32_t logit_dtype; /* SSM_F32 or SSM_BF16 */
+} ssm_accept_desc_t;
+
+/*
+ * ssm_accept_greedy -- accept draft token t while it is the verifier's most
+ * likely token at position t (ties go to the smallest token index);
+ * next_token is the verifier's most likely token at j = accept_len.
+ */
+int ssm_accept_greedy(const ssm_accept_desc_t *desc, const void *target_logits, const int32_t *draft_tokens,
+                      int32_t *accept_len, int32_t *next_token, uint32_t *dev_status, void *stream);
+
+/*
+ * ssm_accept_sample -- speculative sampling: with p_t = softmax(target row t)
+ * and q_t = softmax(draft row t), accept draft token x_t while
+ * uniform[t] < p_t(x_t) / q_t(x_t) (always when q_t(x_t) = 0). At the first
+ * rejection j < ntok the next token is drawn from the normalised residual
+ * max(0, p_j - q_j), after ntok acceptances from p_ntok: the smallest index
+ * whose cumulative weight exceeds uniform[ntok] times the total weight (the
+ * last index of positive weight if rounding leaves none; vocab - 1 if no
+ * weight is positive).
+ */
+int ssm_accept_sample(const ssm_accept_desc_t *desc, const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const float *uniform, int32_t *accept_len, int32_t *next_token,
+                      uint32_t *dev_status, void *stream);
 
 /* A static, human-readable string for an SSM_* return code. */
 const char *ssm_strerror(int code);

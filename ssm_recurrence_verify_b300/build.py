@@ -14,8 +14,8 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SRC = os.path.join(HERE, "csrc", "ssmverify.cu")
-HDR = os.path.join(ROOT, "include", "ssmverify.h")
+SRCS = [os.path.join(HERE, "csrc", n) for n in ("ssmverify.cu", "accept.cu")]
+HDRS = [os.path.join(ROOT, "include", "ssmverify.h"), os.path.join(HERE, "csrc", "ssm_internal.h")]
 LIB = os.path.join(HERE, "libssmverify.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -33,7 +33,7 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in (SRC, HDR, __file__))
+    return all(os.path.getmtime(p) <= t for p in (*SRCS, *HDRS, __file__))
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -41,7 +41,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, *FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC]
+    cmd = [nvcc(), *ARCH, *FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, *SRCS]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)

@@ -51,6 +51,7 @@
 #include <stdint.h>
 
 #include "ssmverify.h"
+#include "ssm_internal.h"
 
 namespace {
 
@@ -1164,6 +1165,10 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
 }
 
 }  // namespace
+
+namespace ssm_internal {
+void set_last_cuda_error(int e) { g_last_cuda_error = e; }
+}  // namespace ssm_internal
 
 extern "C" {
 

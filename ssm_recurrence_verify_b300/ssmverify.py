@@ -13,7 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -31,15 +31,24 @@ SSM_ERR_ALIAS = 5
 SSM_ERR_CUDA = 6
 SSM_STATUS_BAD_ACCEPT_LEN = 1
 SSM_STATUS_TIMEOUT = 2
+SSM_STATUS_BAD_TOKEN = 4
+SSM_ACCEPT_MAX_NTOK = 32
+SSM_ACCEPT_MAX_VOCAB = 1 << 28
 
 EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
-           "ssm_selftest_wait_timeout", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
+           "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample", "ssm_strerror",
+           "ssm_last_cuda_error", "ssm_version")
 
 
 class SsmDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
                 ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("ntok", ctypes.c_int32),
                 ("in_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class AcceptDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("ntok", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("logit_dtype", ctypes.c_int32)]
 
 
 class SsmError(ValueError):
@@ -68,8 +77,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_commit_verify.argtypes = [dp, vp, ctypes.c_int32] + [vp] * 13
     lib.ssm_step.argtypes = [dp] + [vp] * 10
     lib.ssm_selftest_wait_timeout.argtypes = [vp, vp]
+    ap = ctypes.POINTER(AcceptDesc)
+    lib.ssm_accept_greedy.argtypes = [ap] + [vp] * 6
+    lib.ssm_accept_sample.argtypes = [ap] + [vp] * 8
     for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
-              "ssm_selftest_wait_timeout", "ssm_last_cuda_error", "ssm_version"):
+              "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample", "ssm_last_cuda_error",
+              "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
     lib.ssm_strerror.restype = ctypes.c_char_p
@@ -222,3 +235,74 @@ def step(state, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torc
     _check(load_library().ssm_step(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
                                    _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
+
+
+# ----------------------------------------------------------------------------- acceptance
+
+def _accept_validate(target_logits, draft_tokens, draft_logits, uniform, accept_len, next_token):
+    dev = target_logits.device
+    tensors = {"target_logits": target_logits, "draft_tokens": draft_tokens}
+    for k, v in (("draft_logits", draft_logits), ("uniform", uniform), ("accept_len", accept_len),
+                 ("next_token", next_token)):
+        if v is not None:
+            tensors[k] = v
+    for k, v in tensors.items():
+        if not v.is_cuda or v.device != dev:
+            raise ValueError(f"{k} must be a CUDA tensor on {dev}")
+        if not v.is_contiguous():
+            raise ValueError(f"{k} must be contiguous")
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [batch][K+1][V]")
+    bsz, K1, V = target_logits.shape
+    K = K1 - 1
+    if target_logits.dtype == torch.float32:
+        dt = SSM_F32
+    elif target_logits.dtype == torch.bfloat16:
+        dt = SSM_BF16
+    else:
+        raise ValueError(f"logits must be float32 or bfloat16, got {target_logits.dtype}")
+    if draft_tokens.dtype != torch.int32 or tuple(draft_tokens.shape) != (bsz, K):
+        raise ValueError(f"draft_tokens must be int32 [batch][K] = [{bsz}][{K}]")
+    if draft_logits is not None and (draft_logits.dtype != target_logits.dtype
+                                     or tuple(draft_logits.shape) != (bsz, K, V)):
+        raise ValueError(f"draft_logits must be {target_logits.dtype} [batch][K][V] = [{bsz}][{K}][{V}]")
+    if uniform is not None and (uniform.dtype != torch.float32 or tuple(uniform.shape) != (bsz, K1)):
+        raise ValueError(f"uniform must be float32 [batch][K+1] = [{bsz}][{K1}]")
+    for k, v in (("accept_len", accept_len), ("next_token", next_token)):
+        if v is not None and (v.dtype != torch.int32 or tuple(v.shape) != (bsz,)):
+            raise ValueError(f"{k} must be int32 [batch]")
+    return AcceptDesc(bsz, K, V, dt)
+
+
+def _accept_outputs(target_logits, accept_len, next_token):
+    bsz = target_logits.shape[0]
+    dev = target_logits.device
+    if accept_len is None:
+        accept_len = torch.empty(bsz, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(bsz, dtype=torch.int32, device=dev)
+    return accept_len, next_token
+
+
+def accept_greedy(target_logits, draft_tokens, accept_len=None, next_token=None, dev_status=None,
+                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Greedy acceptance on the device: ``(accept_len, next_token)``, int32
+    [batch] each. target_logits [batch][K+1][V] (fp32 or bf16), draft_tokens
+    int32 [batch][K]."""
+    accept_len, next_token = _accept_outputs(target_logits, accept_len, next_token)
+    desc = _accept_validate(target_logits, draft_tokens, None, None, accept_len, next_token)
+    _check(load_library().ssm_accept_greedy(ctypes.byref(desc), _ptr(target_logits), _ptr(draft_tokens),
+                                            _ptr(accept_len), _ptr(next_token), _ptr(dev_status), _stream(stream)))
+    return accept_len, next_token
+
+
+def accept_sample(target_logits, draft_logits, draft_tokens, uniform, accept_len=None, next_token=None,
+                  dev_status=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Speculative sampling on the device: ``(accept_len, next_token)``.
+    draft_logits [batch][K][V] (the target's dtype), uniform fp32 [batch][K+1]."""
+    accept_len, next_token = _accept_outputs(target_logits, accept_len, next_token)
+    desc = _accept_validate(target_logits, draft_tokens, draft_logits, uniform, accept_len, next_token)
+    _check(load_library().ssm_accept_sample(ctypes.byref(desc), _ptr(target_logits), _ptr(draft_logits),
+                                            _ptr(draft_tokens), _ptr(uniform), _ptr(accept_len), _ptr(next_token),
+                                            _ptr(dev_status), _stream(stream)))
+    return accept_len, next_token

@@ -238,3 +238,77 @@ def test_commit_verify_validation(lib):
 def test_selftest_validation(lib):
     assert lib.ssm_selftest_wait_timeout(None, None) == sv.SSM_ERR_NULL
     assert lib.ssm_selftest_wait_timeout(ctypes.c_void_p(BASE + 2), None) == sv.SSM_ERR_ALIGN
+
+
+def adesc(**kw):
+    d = dict(batch=2, ntok=3, vocab=1000, logit_dtype=sv.SSM_BF16)
+    d.update(kw)
+    return sv.AcceptDesc(**d)
+
+
+def ag(lib, d, p):
+    """ssm_accept_greedy(desc, target_logits, draft_tokens, accept_len, next_token, dev_status, stream)."""
+    return lib.ssm_accept_greedy(ctypes.byref(d) if d is not None else None, *p, None)
+
+
+def asa(lib, d, p):
+    """ssm_accept_sample(desc, target_logits, draft_logits, draft_tokens, uniform, accept_len, next_token,
+    dev_status, stream)."""
+    return lib.ssm_accept_sample(ctypes.byref(d) if d is not None else None, *p, None)
+
+
+@no_gpu_only
+def test_accept_validation(lib):
+    assert ag(lib, None, ptrs(5)) == sv.SSM_ERR_NULL
+    assert asa(lib, None, ptrs(7)) == sv.SSM_ERR_NULL
+    for i in range(4):  # dev_status alone is optional
+        p = ptrs(5)
+        p[i] = None
+        assert ag(lib, adesc(), p) == sv.SSM_ERR_NULL, i
+    for i in range(6):
+        p = ptrs(7)
+        p[i] = None
+        assert asa(lib, adesc(), p) == sv.SSM_ERR_NULL, i
+    for kw, code in ((dict(ntok=0), sv.SSM_ERR_SHAPE), (dict(ntok=sv.SSM_ACCEPT_MAX_NTOK + 1), sv.SSM_ERR_SHAPE),
+                     (dict(vocab=0), sv.SSM_ERR_SHAPE), (dict(vocab=sv.SSM_ACCEPT_MAX_VOCAB + 1), sv.SSM_ERR_SHAPE),
+                     (dict(batch=-1), sv.SSM_ERR_SHAPE), (dict(logit_dtype=5), sv.SSM_ERR_UNSUPPORTED)):
+        assert ag(lib, adesc(**kw), ptrs(5)) == code, kw
+        assert asa(lib, adesc(**kw), ptrs(7)) == code, kw
+    # alignment: logits to their element size, the int32 / float arrays to 4 bytes
+    for i, off in [(0, 1), (1, 2), (2, 2), (3, 2), (4, 2)]:
+        p = ptrs(5)
+        p[i] = ctypes.c_void_p(p[i].value + off)
+        assert ag(lib, adesc(), p) == sv.SSM_ERR_ALIGN, i
+    for i, off in [(0, 1), (1, 1), (2, 2), (3, 2), (4, 2), (5, 2), (6, 2)]:
+        p = ptrs(7)
+        p[i] = ctypes.c_void_p(p[i].value + off)
+        assert asa(lib, adesc(), p) == sv.SSM_ERR_ALIGN, i
+    p = ptrs(5)
+    p[0] = ctypes.c_void_p(p[0].value + 2)            # 2 bytes suffice for bf16 logits, not for fp32
+    assert ag(lib, adesc(logit_dtype=sv.SSM_F32), p) == sv.SSM_ERR_ALIGN
+    assert ag(lib, adesc(), p) == sv.SSM_ERR_CUDA     # valid: with no device here the launch fails
+    # aliasing: outputs against inputs and each other
+    p = ptrs(5)
+    p[2] = ctypes.c_void_p(p[1].value + 4)            # accept_len inside draft_tokens
+    assert ag(lib, adesc(), p) == sv.SSM_ERR_ALIAS
+    p = ptrs(5)
+    p[3] = p[2]                                        # next_token on accept_len
+    assert ag(lib, adesc(), p) == sv.SSM_ERR_ALIAS
+    p = ptrs(7)
+    p[6] = ctypes.c_void_p(p[5].value + 4)            # dev_status inside next_token
+    assert asa(lib, adesc(), p) == sv.SSM_ERR_ALIAS
+    p = ptrs(7)
+    p[4] = ctypes.c_void_p(p[1].value + 64)           # accept_len inside the draft logits
+    assert asa(lib, adesc(), p) == sv.SSM_ERR_ALIAS
+    p = ptrs(7)
+    p[1] = p[0]                                        # read-only inputs may overlap
+    assert asa(lib, adesc(), p) == sv.SSM_ERR_CUDA
+    # an empty batch inspects no pointer
+    assert ag(lib, adesc(batch=0), [None] * 5) == sv.SSM_OK
+    assert asa(lib, adesc(batch=0), [None] * 7) == sv.SSM_OK
+
+
+def test_accept_shim_checks_shapes():
+    t = torch.zeros(2, 4, 10)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sv.accept_greedy(t, torch.zeros(2, 3, dtype=torch.int32))
