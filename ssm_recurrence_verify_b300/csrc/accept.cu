@@ -42,6 +42,7 @@
 #include <cooperative_groups.h>
 
 #include <climits>
+#include <type_traits>
 #include <stdint.h>
 
 #include "ssmverify.h"
@@ -53,7 +54,7 @@ namespace {
 
 constexpr int kAT = 256;                             // threads per CTA
 constexpr int kAWarps = kAT / 32;
-constexpr int kAU = 8;                               // 16-byte loads in flight per thread and row
+constexpr int kAU = 8;                               // 16-byte loads in flight per thread and batch
 constexpr int kAS = 16;                              // elements per thread and batch on the scalar path
 constexpr int kCl = 8;                               // CTAs per sequence (one cluster)
 constexpr int kMaxRows = 2 * SSM_ACCEPT_MAX_NTOK + 1;
@@ -102,8 +103,19 @@ struct Logit<float> {
     static constexpr uint32_t kNegInf = 0xff800000u;     // one -inf per word
     __device__ static float get(const uint4 &r, int l) { return __uint_as_float(word(r, l)); }
     __device__ static float one(const float *p) { return __ldg(p); }
-    __device__ static float vmax(const uint4 &r) {
-        return fmaxf(fmaxf(get(r, 0), get(r, 1)), fmaxf(get(r, 2), get(r, 3)));
+    __device__ static float2 pair(const uint4 &r, int q) {  // elements 2q, 2q + 1
+        return q == 0 ? make_float2(__uint_as_float(r.x), __uint_as_float(r.y))
+                      : make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
+    template <int S>
+    __device__ static float bmax(const uint4 (&r)[S]) {
+        float m0 = fmaxf(get(r[0], 0), get(r[0], 1)), m1 = fmaxf(get(r[0], 2), get(r[0], 3));
+#pragma unroll
+        for (int k = 1; k < S; ++k) {
+            m0 = fmaxf(m0, fmaxf(get(r[k], 0), get(r[k], 1)));
+            m1 = fmaxf(m1, fmaxf(get(r[k], 2), get(r[k], 3)));
+        }
+        return fmaxf(m0, m1);
     }
 };
 
@@ -127,49 +139,68 @@ struct Logit<__nv_bfloat16> {
         __builtin_memcpy(&r, &m, 4);
         return r;
     }
-    __device__ static float vmax(const uint4 &r) {
-        const uint32_t m = max2(max2(r.x, r.y), max2(r.z, r.w));
+    __device__ static float2 pair(const uint4 &r, int q) {  // elements 2q, 2q + 1
+        const uint32_t w = word(r, q);
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    template <int S>
+    __device__ static float bmax(const uint4 (&r)[S]) {  // packed bf16x2 maxima, unpacked once
+        uint32_t m0 = max2(r[0].x, r[0].y), m1 = max2(r[0].z, r[0].w);
+#pragma unroll
+        for (int k = 1; k < S; ++k) {
+            m0 = max2(m0, max2(r[k].x, r[k].y));
+            m1 = max2(m1, max2(r[k].z, r[k].w));
+        }
+        const uint32_t m = max2(m0, m1);
         return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
     }
 };
 
 // A batch of logits of one row seen by one thread, in increasing index order
-// (slot k, element l). Masked-out entries read -inf. Slot 0 is always valid.
+// (slot k, element l). Masked-out entries read -inf; valid slots come first,
+// and a batch whose slot 0 is masked (any == false) holds nothing.
 template <typename T, bool VEC>
 struct Batch;
 
 template <typename T>
 struct Batch<T, true> {
     static constexpr int S = kAU, W = Logit<T>::W;
+    static constexpr bool kPaired = true;
     uint4 r[S];
-    int v0;  // vector index of slot 0
+    int v0;     // vector index of slot 0
+    bool any;   // slot 0 (and so the batch) holds data
     __device__ void load(const T *row, int v0_, int vhi) {
         v0 = v0_;
+        any = v0 < vhi;
         const uint4 *p = reinterpret_cast<const uint4 *>(row);
+        if (v0 + (S - 1) * kAT < vhi) {  // the usual case: every slot inside the slice
 #pragma unroll
-        for (int k = 0; k < S; ++k) {
-            const int v = v0 + k * kAT;
-            r[k] = v < vhi ? ld_stream(p + v) : make_uint4(Logit<T>::kNegInf, Logit<T>::kNegInf, Logit<T>::kNegInf,
-                                                           Logit<T>::kNegInf);
+            for (int k = 0; k < S; ++k) r[k] = ld_stream(p + v0 + k * kAT);
+        } else {
+            const uint4 neg = make_uint4(Logit<T>::kNegInf, Logit<T>::kNegInf, Logit<T>::kNegInf, Logit<T>::kNegInf);
+#pragma unroll
+            for (int k = 0; k < S; ++k) {
+                const int v = v0 + k * kAT;
+                r[k] = v < vhi ? ld_stream(p + v) : neg;
+            }
         }
     }
     __device__ float get(int k, int l) const { return Logit<T>::get(r[k], l); }
+    __device__ float2 pair(int k, int q) const { return Logit<T>::pair(r[k], q); }
     __device__ int index(int k, int l) const { return (v0 + k * kAT) * W + l; }
-    __device__ float bmax() const {
-        float m = Logit<T>::vmax(r[0]);
-#pragma unroll
-        for (int k = 1; k < S; ++k) m = fmaxf(m, Logit<T>::vmax(r[k]));
-        return m;
-    }
+    __device__ float bmax() const { return Logit<T>::template bmax<S>(r); }
 };
 
 template <typename T>
 struct Batch<T, false> {
     static constexpr int S = kAS, W = 1;
+    static constexpr bool kPaired = false;
     float r[S];
     int e0;
+    bool any;
     __device__ void load(const T *row, int e0_, int ehi) {
         e0 = e0_;
+        any = e0 < ehi;
 #pragma unroll
         for (int k = 0; k < S; ++k) {
             const int e = e0 + k * kAT;
@@ -177,6 +208,7 @@ struct Batch<T, false> {
         }
     }
     __device__ float get(int k, int) const { return r[k]; }
+    __device__ float2 pair(int, int) const { return make_float2(0.f, 0.f); }  // not used (kPaired is false)
     __device__ int index(int k, int) const { return e0 + k * kAT; }
     __device__ float bmax() const {
         float m = r[0];
@@ -191,28 +223,44 @@ struct SoftAcc {
     float m = kEmpty, s = 0.f;
     template <class B>
     __device__ void push(const B &b) {
+        if (!b.any) return;
         const float bm = b.bmax();
         if (bm > m) {
             s *= exp2_ftz((m - bm) * kLog2e);
             m = bm;
         }
         const float nml = -(m * kLog2e);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        if constexpr (B::kPaired) {
+            // two entries per instruction for the exponent argument and the sum
+            const float2 l2 = make_float2(kLog2e, kLog2e), n2 = make_float2(nml, nml);
+            float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
-        for (int k = 0; k < B::S; ++k) {
+            for (int k = 0; k < B::S; ++k) {
 #pragma unroll
-            for (int l = 0; l < B::W; l += 1) {
-                const float e = exp2_ftz(fmaf(b.get(k, l), kLog2e, nml));
-                switch ((k * B::W + l) & 3) {
-                    case 0: a0 += e; break;
-                    case 1: a1 += e; break;
-                    case 2: a2 += e; break;
-                    default: a3 += e; break;
+                for (int q = 0; q < B::W / 2; ++q) {
+                    const float2 x = __ffma2_rn(b.pair(k, q), l2, n2);
+                    const float2 e = make_float2(exp2_ftz(x.x), exp2_ftz(x.y));
+                    if ((k * (B::W / 2) + q) & 1)
+                        a1 = __fadd2_rn(a1, e);
+                    else
+                        a0 = __fadd2_rn(a0, e);
                 }
             }
+            s += (a0.x + a1.x) + (a0.y + a1.y);
+        } else {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < B::S; ++k) {
+                const float e = exp2_ftz(fmaf(b.get(k, 0), kLog2e, nml));
+                if (k & 1)
+                    a1 += e;
+                else
+                    a0 += e;
+            }
+            s += a0 + a1;
         }
-        s += (a0 + a1) + (a2 + a3);
     }
+    __device__ float2 warp_total();
 };
 
 __device__ __forceinline__ void soft_combine(float &m, float &s, float m2, float s2) {
@@ -221,12 +269,20 @@ __device__ __forceinline__ void soft_combine(float &m, float &s, float m2, float
     m = M;
 }
 
+__device__ __forceinline__ float2 SoftAcc::warp_total() {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        soft_combine(m, s, __shfl_xor_sync(~0u, m, off), __shfl_xor_sync(~0u, s, off));
+    return make_float2(m, s);
+}
+
 // Running argmax: the largest value and the smallest index holding it.
 struct ArgAcc {
     float v = -INFINITY;
     int i = kNoIndex;
     template <class B>
     __device__ void push(const B &b) {
+        if (!b.any) return;
         const float bm = b.bmax();
         if (bm > v || (i == kNoIndex && bm == v)) {
             int idx = kNoIndex;
@@ -240,6 +296,7 @@ struct ArgAcc {
             i = idx;
         }
     }
+    __device__ float2 warp_total();
 };
 
 __device__ __forceinline__ void arg_combine(float &v, int &i, float v2, int i2) {
@@ -247,6 +304,13 @@ __device__ __forceinline__ void arg_combine(float &v, int &i, float v2, int i2) 
         v = v2;
         i = i2;
     }
+}
+
+__device__ __forceinline__ float2 ArgAcc::warp_total() {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        arg_combine(v, i, __shfl_xor_sync(~0u, v, off), __shfl_xor_sync(~0u, i, off));
+    return make_float2(v, __int_as_float(i));
 }
 
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
@@ -264,6 +328,18 @@ struct Weigher {
         const float q = __fmul_rn(exp2_ftz(fmaf(lq, kLog2e, nmlq)), invq);
         return fmaxf(__fsub_rn(p, q), 0.f);
     }
+    // The same weights for two neighbouring entries, two per instruction
+    // (each lane rounds exactly as the scalar form does).
+    __device__ float2 pair(float2 lp, float2 lq) const {
+        const float2 l2 = make_float2(kLog2e, kLog2e);
+        const float2 xp = __ffma2_rn(lp, l2, make_float2(nmlp, nmlp));
+        const float2 p = __fmul2_rn(make_float2(exp2_ftz(xp.x), exp2_ftz(xp.y)), make_float2(invp, invp));
+        if (!resid) return p;
+        const float2 xq = __ffma2_rn(lq, l2, make_float2(nmlq, nmlq));
+        const float2 q = __fmul2_rn(make_float2(exp2_ftz(xq.x), exp2_ftz(xq.y)), make_float2(invq, invq));
+        const float2 d = __ffma2_rn(q, make_float2(-1.f, -1.f), p);  // p - q, one rounding
+        return make_float2(fmaxf(d.x, 0.f), fmaxf(d.y, 0.f));
+    }
 };
 
 // Walk the run [e_lo, e_hi) of a row in index order, accumulating the weights
@@ -274,8 +350,7 @@ template <typename T, bool VEC, bool FIND>
 __device__ float run_weights(const T *prow, const T *qrow, int e_lo, int e_hi, const Weigher &wf, float P, float Tk,
                              float thr, int &first, int &last) {
     float part = 0.f;
-    auto visit = [&](float lp, float lq, int e) {
-        const float w = wf(lp, lq);
+    auto visit = [&](float w, int e) {
         part = __fadd_rn(part, w);
         if (FIND) {
             if (w > 0.f) {
@@ -285,28 +360,44 @@ __device__ float run_weights(const T *prow, const T *qrow, int e_lo, int e_hi, c
         }
     };
     if (VEC) {
-        constexpr int W = Logit<T>::W;
+        // groups of two vectors per row, the next group's loads issued before
+        // the current group is consumed
+        constexpr int W = Logit<T>::W, G = 2;
         const uint4 *pv = reinterpret_cast<const uint4 *>(prow);
         const uint4 *qv = reinterpret_cast<const uint4 *>(qrow);
-        for (int v = e_lo / W; v < e_hi / W; v += 4) {
-            uint4 rp[4], rq[4];
+        const int vlo = e_lo / W, vhi = e_hi / W;
+        uint4 cp[G], cq[G], np_[G], nq[G];
+        auto fetch = [&](uint4 (&rp)[G], uint4 (&rq)[G], int v) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const bool ok = v + k < e_hi / W;
+            for (int k = 0; k < G; ++k) {
+                const bool ok = v + k < vhi;
                 rp[k] = ok ? __ldg(pv + v + k) : make_uint4(0, 0, 0, 0);
                 rq[k] = ok && wf.resid ? __ldg(qv + v + k) : make_uint4(0, 0, 0, 0);
             }
+        };
+        if (vlo < vhi) fetch(cp, cq, vlo);
+        for (int v = vlo; v < vhi; v += G) {
+            if (v + G < vhi) fetch(np_, nq, v + G);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (v + k >= e_hi / W) break;
+            for (int k = 0; k < G; ++k) {
+                if (v + k >= vhi) break;
 #pragma unroll
-                for (int l = 0; l < W; ++l)
-                    visit(Logit<T>::get(rp[k], l), Logit<T>::get(rq[k], l), (v + k) * W + l);
+                for (int q = 0; q < W / 2; ++q) {
+                    const float2 w = wf.pair(Logit<T>::pair(cp[k], q), Logit<T>::pair(cq[k], q));
+                    const int e = (v + k) * W + 2 * q;
+                    visit(w.x, e);
+                    visit(w.y, e + 1);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < G; ++k) {
+                cp[k] = np_[k];
+                cq[k] = nq[k];
             }
         }
     } else {
         for (int e = e_lo; e < e_hi; ++e)
-            visit(Logit<T>::one(prow + e), wf.resid ? Logit<T>::one(qrow + e) : 0.f, e);
+            visit(wf(Logit<T>::one(prow + e), wf.resid ? Logit<T>::one(qrow + e) : 0.f), e);
     }
     return part;
 }
@@ -332,60 +423,44 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
     const int lo = min(rank * a.slice, V), hi = min(lo + a.slice, V);
     constexpr int W = VEC ? Logit<T>::W : 1;
 
+    // ---- phase 0: the logits at the draft tokens, which the acceptance
+    // rule reads; loaded now (warp 0, one token per lane), used after phase 1.
+    int pre_x = -1;
+    float pre_lp = 0.f, pre_lq = 0.f, pre_u = 0.f;
+    if (warp == 0 && lane < K) {
+        pre_x = a.drafts[(int64_t)b * K + lane];
+        if (SAMPLE) pre_u = a.u[(int64_t)b * (K + 1) + lane];
+        if (SAMPLE && pre_x >= 0 && pre_x < V) {
+            pre_lp = Logit<T>::one(tl + (int64_t)lane * V + pre_x);
+            pre_lq = Logit<T>::one(ql + (int64_t)lane * V + pre_x);
+        }
+    }
+
     // ---- phase 1: per-row partials of this CTA's slice. Rows run from the
     // bonus position down to 0 so that the rows a rejection most often picks
     // are the most recently read when the next-token draw re-reads them.
-    for (int step = 0; step < R; ++step) {
-        int row;  // index into the partial arrays: t for verifier row t, K + 1 + t for draft row t
-        const T *src;
-        if (step == 0) {
-            row = K;
-        } else {
-            const int t = K - 1 - (step - 1) / (SAMPLE ? 2 : 1);
-            row = (SAMPLE && ((step - 1) & 1) == 0) ? K + 1 + t : t;
-        }
-        src = row <= K ? tl + (int64_t)row * V : ql + (int64_t)(row - K - 1) * V;
-        float2 out;
-        if (SAMPLE) {
-            SoftAcc acc;
-            if (VEC) {
-                for (int v0 = lo / W + tid; v0 < hi / W; v0 += kAU * kAT) {
-                    Batch<T, VEC> bt;
-                    bt.load(src, v0, hi / W);
-                    acc.push(bt);
-                }
+    {
+        using Bt = Batch<T, VEC>;
+        using Acc = typename std::conditional<SAMPLE, SoftAcc, ArgAcc>::type;
+        const int ulo = lo / W, uhi = hi / W;  // slice in load units (vectors, or elements)
+        for (int step = 0; step < R; ++step) {
+            int row;  // t for verifier row t, K + 1 + t for draft row t
+            if (step == 0) {
+                row = K;
             } else {
-                for (int e0 = lo + tid; e0 < hi; e0 += kAS * kAT) {
-                    Batch<T, VEC> bt;
-                    bt.load(src, e0, hi);
-                    acc.push(bt);
-                }
+                const int t = K - 1 - (step - 1) / (SAMPLE ? 2 : 1);
+                row = (SAMPLE && ((step - 1) & 1) == 0) ? K + 1 + t : t;
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                soft_combine(acc.m, acc.s, __shfl_xor_sync(~0u, acc.m, off), __shfl_xor_sync(~0u, acc.s, off));
-            out = make_float2(acc.m, acc.s);
-        } else {
-            ArgAcc acc;
-            if (VEC) {
-                for (int v0 = lo / W + tid; v0 < hi / W; v0 += kAU * kAT) {
-                    Batch<T, VEC> bt;
-                    bt.load(src, v0, hi / W);
-                    acc.push(bt);
-                }
-            } else {
-                for (int e0 = lo + tid; e0 < hi; e0 += kAS * kAT) {
-                    Batch<T, VEC> bt;
-                    bt.load(src, e0, hi);
-                    acc.push(bt);
-                }
+            const T *src = row <= K ? tl + (int64_t)row * V : ql + (int64_t)(row - K - 1) * V;
+            Acc acc;
+            for (int u0 = ulo + tid; u0 < uhi; u0 += Bt::S * kAT) {
+                Bt bt;
+                bt.load(src, u0, uhi);
+                acc.push(bt);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                arg_combine(acc.v, acc.i, __shfl_xor_sync(~0u, acc.v, off), __shfl_xor_sync(~0u, acc.i, off));
-            out = make_float2(acc.v, __int_as_float(acc.i));
+            const float2 out = acc.warp_total();
+            if (lane == 0) wpart[row][warp] = out;
         }
-        if (lane == 0) wpart[row][warp] = out;
     }
     __syncthreads();
     if (tid < R) {
@@ -422,34 +497,25 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
 
     // ---- phase 3: accept while the rule holds (warp 0; the same in every CTA)
     if (warp == 0) {
-        int j = K, badj = 0;
-        for (int t0 = 0; t0 < K; t0 += 32) {
-            const int t = t0 + lane;
-            bool rej = false, bad = false;
-            if (t < K) {
-                const int x = a.drafts[(int64_t)b * K + t];
-                bad = x < 0 || x >= V;
-                if (bad) {
-                    rej = true;
-                } else if (!SAMPLE) {
-                    rej = __float_as_int(fin[t].y) != x;
-                } else {
-                    const float2 fp = fin[t], fq = fin[K + 1 + t];
-                    const float ep = exp2_ftz(fmaf(Logit<T>::one(tl + (int64_t)t * V + x), kLog2e, -(fp.x * kLog2e)));
-                    const float eq = exp2_ftz(fmaf(Logit<T>::one(ql + (int64_t)t * V + x), kLog2e, -(fq.x * kLog2e)));
-                    const float p = __fdiv_rn(ep, fp.y), q = __fdiv_rn(eq, fq.y);
-                    const float ratio = q > 0.f ? __fdiv_rn(p, q) : INFINITY;
-                    rej = !(a.u[(int64_t)b * (K + 1) + t] < ratio);
-                }
-            }
-            const unsigned m = __ballot_sync(~0u, rej);
-            if (m != 0u) {
-                const int first = __ffs(m) - 1;
-                j = t0 + first;
-                badj = __shfl_sync(~0u, bad ? 1 : 0, first);
-                break;
+        bool rej = false, bad = false;
+        if (lane < K) {
+            bad = pre_x < 0 || pre_x >= V;
+            if (bad) {
+                rej = true;
+            } else if (!SAMPLE) {
+                rej = __float_as_int(fin[lane].y) != pre_x;
+            } else {
+                const float2 fp = fin[lane], fq = fin[K + 1 + lane];
+                const float ep = exp2_ftz(fmaf(pre_lp, kLog2e, -(fp.x * kLog2e)));
+                const float eq = exp2_ftz(fmaf(pre_lq, kLog2e, -(fq.x * kLog2e)));
+                const float p = __fdiv_rn(ep, fp.y), q = __fdiv_rn(eq, fq.y);
+                const float ratio = q > 0.f ? __fdiv_rn(p, q) : INFINITY;
+                rej = !(pre_u < ratio);
             }
         }
+        const unsigned m = __ballot_sync(~0u, rej);
+        const int j = m != 0u ? __ffs(m) - 1 : K;
+        const int badj = m != 0u ? __shfl_sync(~0u, bad ? 1 : 0, j) : 0;
         if (lane == 0) {
             s_j = j;
             s_bad = badj;
