@@ -531,6 +531,95 @@ def run_accept(args, sample: bool, rank, world, local_rank):
     }
 
 
+# ----------------------------------------------------------------------------- prefill
+
+PREFILL_METRIC = "prompt tokens/s per SSM layer (prefill); achieved FP32 TFLOP/s vs B300 peak"
+SM_COUNT, FP32_LANES, SM_MAX_GHZ = 148, 128, 2.032  # B300: the FP32 peak is derived from these
+FP32_PEAK_TFLOPS = SM_COUNT * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+
+
+def run_prefill(args, rank, world, local_rank):
+    """Time ssm_prefill: one Llama-3-8B-shaped layer (H 32, P 128, N 128,
+    G 8), one 2048-token bf16 prompt per GPU, from a zeroed cache slot. The
+    algorithmic work is the recurrence over the prompt: 5 flops per state
+    element and token (u B, Abar h + u B, and y = C h)."""
+    import ssm_recurrence_verify_b300 as ssm
+    from ssm_recurrence_verify_b300 import build as libbuild
+    if not os.path.exists(libbuild.LIB):
+        libbuild.build()
+    ssm.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.custom_workload(1, 32, 128, 128, 8, 2048, synth.BF16, seed=500, accept="all")
+    T = wl.ntok
+    sets = []
+    for i in range(2):
+        d = synth.draw_layer_round(wl, rnd=i)
+        e = {k: v.to(dev) for k, v in d.items()}
+        e["y"] = torch.empty((1, T, wl.nheads, wl.headdim), dtype=torch.float32, device=dev)
+        e["pool"] = torch.zeros(1, wl.nheads, wl.headdim, wl.dstate, device=dev)
+        sets.append(e)
+    nbytes = ssm.prefill_workspace_bytes(sets[0]["pool"], sets[0]["x"], sets[0]["B"], sets[0]["C"], sets[0]["dt"],
+                                         sets[0]["A"], sets[0]["D"])
+    ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(e, chunked=True):
+        ssm.prefill(e["pool"], None, e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], y=e["y"],
+                    workspace=ws if chunked else ws[:0], dev_status=status, stream=stream)
+
+    def timed(chunked, steps):
+        with torch.cuda.stream(stream):
+            for e in sets:
+                launch(e, chunked)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                launch(sets[i % 2], chunked)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / steps
+
+    steps = max(3, min(args.steps, 200))
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    wall0 = time.perf_counter()
+    ms = timed(True, steps)
+    wall1 = time.perf_counter()
+    sampler.stop()
+    ms_one_pass = timed(False, max(3, steps // 4))
+    assert int(status.item()) == 0, "device reported a problem"
+    ms_max = max_over_ranks(ms, world)
+    flops = 5.0 * T * wl.nheads * wl.headdim * wl.dstate
+    achieved = flops / (ms * 1e-3) / 1e12
+    io_bytes = T * (wl.nheads * wl.headdim * (2 + 4) + 2 * wl.ngroups * wl.dstate * 2 + wl.nheads * 2) \
+        + 2 * wl.nheads * wl.headdim * wl.dstate * 4
+    return {
+        "metric": PREFILL_METRIC, "value": T * world / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": 3, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": "prefill_llama3_8b_layer_b1_t2048_h32_p128_n128_g8", "prompt_tokens": T,
+                   "batch_per_gpu": 1, "in_dtype": "bf16", "workspace_bytes": nbytes,
+                   "timing": f"{steps} launches captured in one CUDA graph, 2 input sets alternating"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 flops x 2.032 GHz",
+                     "algorithmic_flops_per_step": flops,
+                     "hbm_gbs_on_io_bytes": io_bytes / (ms * 1e-3) / 1e9},
+        "one_pass_ms": ms_one_pass,
+        "gpu_launches": steps, "clocks": sampler.summary(wall0, wall1),
+    }
+
+
 # ----------------------------------------------------------------------------- oracle (CPU) legs
 
 def oracle_throughput(wl, seconds: float, max_seqs: int = None):
@@ -633,8 +722,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy"], default="ssm",
-                    help="ssm: the verify/commit step (default); accept_*: the acceptance step alone")
+    ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill"], default="ssm",
+                    help="ssm: the verify/commit step (default); accept_*: the acceptance step alone; "
+                         "prefill: a 2048-token prompt through one layer")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -648,7 +738,10 @@ def main(argv=None):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.path != "ssm":
-        line = run_accept(args, args.path == "accept_sample", rank, world, local_rank)
+        if args.path == "prefill":
+            line = run_prefill(args, rank, world, local_rank)
+        else:
+            line = run_accept(args, args.path == "accept_sample", rank, world, local_rank)
         if rank == 0:
             print(json.dumps(line), flush=True)
         if world > 1:

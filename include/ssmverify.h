@@ -39,7 +39,7 @@
  * nothing, frees nothing and never synchronises; the only state it keeps
  * between calls is a cache of immutable device properties (SM count and
  * resident blocks per SM, per kernel and device), so calls are thread-safe.
- * Every entry point only validates its arguments and enqueues one kernel on
+ * Every entry point only validates its arguments and enqueues one kernel (ssm_prefill: up to three) on
  * `stream` (a cudaStream_t passed as void*, NULL = the legacy default
  * stream) on the current device. Calls are asynchronous.
  *
@@ -93,6 +93,7 @@ extern "C" {
 #define SSM_STATUS_BAD_ACCEPT_LEN 1u
 #define SSM_STATUS_TIMEOUT 2u
 #define SSM_STATUS_BAD_TOKEN 4u /* acceptance: a draft token outside [0, vocab) */
+#define SSM_STATUS_BAD_SLOT 8u  /* pool: a sequence's slot outside [0, nslots) */
 
 typedef struct {
     int32_t batch;    /* sequences */
@@ -164,6 +165,72 @@ int ssm_commit_verify(const ssm_desc_t *desc, float *state, int32_t prev_ntok, c
  */
 int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B, const void *C,
              const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * State pool (serving) and prefill.
+ *
+ * A serving loop keeps the cached states of its live sequences in a pool and
+ * runs each step on whichever sequences are scheduled: sequence b of a call
+ * uses pool slot slot[b]. The pool variants below are the entry points
+ * above with `state` replaced by a pool; everything else (layouts of the
+ * inputs and y, accept_len, errors) is unchanged. A slot outside
+ * [0, nslots) leaves that sequence's y and state unwritten and ORs
+ * SSM_STATUS_BAD_SLOT into *dev_status. Two sequences of one call must not
+ * share a slot (their updates would race; nothing checks this on the device).
+ *
+ * Prefill runs a prompt through the layer and leaves the state at its last
+ * token in the cache: the state the speculative rounds start from (the
+ * speculative-decoding section's cached state; the method overview's
+ * recurrence applied token after token). It equals ssm_verify_commit with
+ * every token accepted; for long prompts on few sequences it splits the
+ * prompt into chunks and runs them side by side (each chunk's state from
+ * h = 0, a scan that carries the state across the chunks, then every chunk's
+ * outputs from the state it starts from), which regroups the same
+ * recurrence and agrees with it to fp32 rounding.
+ * ------------------------------------------------------------------------ */
+
+typedef struct {
+    float *states;        /* [nslots][nheads][headdim][dstate] fp32, 16-byte aligned */
+    const int32_t *slot;  /* [batch] slot of each sequence, device memory; NULL: sequence b uses slot b */
+    int32_t nslots;       /* >= 1; >= batch when slot is NULL */
+    int32_t reserved;     /* must be 0 */
+} ssm_pool_t;
+
+int ssm_verify_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                    const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
+int ssm_commit_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *dt,
+                    const float *A, const int32_t *accept_len, uint32_t *dev_status, void *stream);
+int ssm_verify_commit_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B,
+                           const void *C, const void *dt, const float *A, const float *D, const int32_t *accept_len,
+                           float *y, uint32_t *dev_status, void *stream);
+int ssm_commit_verify_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, int32_t prev_ntok, const void *x_prev,
+                           const void *B_prev, const void *dt_prev, const int32_t *accept_len_prev, const void *x,
+                           const void *B, const void *C, const void *dt, const float *A, const float *D, float *y,
+                           uint32_t *dev_status, void *stream);
+int ssm_step_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                  const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
+
+/*
+ * ssm_prefill_workspace_bytes -- device workspace that ssm_prefill would use
+ * for this shape on the current device (0: it runs in one pass and needs
+ * none): batch * (ntok / L) states for the chunk length L it picks, plus a
+ * small map of the chunks' slots.
+ */
+int64_t ssm_prefill_workspace_bytes(const ssm_desc_t *desc);
+
+/*
+ * ssm_prefill -- run desc->ntok prompt tokens of every sequence from its
+ * cached state (pool slot; zero it first for a fresh prompt), write y for
+ * every token and leave the state after the last token in the slot. x, B, C,
+ * dt, y have the layouts above with ntok = prompt length. `workspace`
+ * (device, 16-byte aligned, workspace_bytes long; may be NULL) lets the
+ * prompt be chunked; with too little workspace the call takes the one-pass
+ * form (same results to rounding). The workspace must not overlap any other
+ * buffer. Launches up to three kernels on `stream`.
+ */
+int ssm_prefill(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                const void *dt, const float *A, const float *D, float *y, void *workspace, int64_t workspace_bytes,
+                uint32_t *dev_status, void *stream);
 
 /*
  * ssm_selftest_wait_timeout -- failure-detection self-test of the bounded

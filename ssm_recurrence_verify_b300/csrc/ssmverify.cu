@@ -142,6 +142,9 @@ struct Block {
 struct Args {
     const float *state_in;  // state read by the tile loads
     float *state;           // state written (nullptr for verify)
+    const int32_t *slot;    // pool slot of each sequence (nullptr: sequence b uses slot b)
+    int nslots;             // slots in the pool (with slot != nullptr)
+    int zero_state;         // every tile starts from h = 0 (no state is read)
     Block ver;              // verify block: y for every token
     Block rep;              // replay block: advanced over its accepted prefix
     const float *A, *D;
@@ -349,6 +352,7 @@ struct Tile {
     long long b;
     int h, g, row0, rows;  // rows: valid rows of this tile (<= kRows)
     long long sbase;       // element offset of the (b, h) state slice
+    bool ok;               // the sequence's pool slot is valid (else nothing is written)
 };
 
 __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, int N) {
@@ -361,7 +365,14 @@ __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, in
     T.g = T.h / (a.H / a.G);
     T.row0 = ptile * kRows;
     T.rows = min(kRows, a.P - T.row0);
-    T.sbase = (T.b * a.H + T.h) * (long long)a.P * N;
+    long long sb = T.b;
+    T.ok = true;
+    if (a.slot != nullptr) {
+        const int s = __ldg(a.slot + T.b);
+        T.ok = s >= 0 && s < a.nslots;
+        sb = T.ok ? s : 0;  // an invalid slot reads slot 0 (in bounds) and writes nothing
+    }
+    T.sbase = (sb * a.H + T.h) * (long long)a.P * N;
     return T;
 }
 
@@ -687,6 +698,7 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
 template <int F>
 __device__ __forceinline__ long long next_work(const Args &a, long long t) {
     if constexpr (F == kCommit) {
+        if (a.accept_len == nullptr) return t;  // every token of every sequence
         const long long per_b = (long long)a.H * a.ptiles;
         for (; t < a.ntiles; t += gridDim.x) {
             const int j = __ldg(a.accept_len + t / per_b);
@@ -754,11 +766,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.b, a.rep.K), kTC) : 0;
         const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
         const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
-        pl.total = (uint32_t)T.rows * N * 4 + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
+        pl.total = (a.zero_state ? 0u : (uint32_t)T.rows * N * 4) + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
         const int ncopy = 1 + 2 * tcR + 3 * tcV;
         const int i = warp + 4 * lane;
         if (i >= ncopy) return pl;
         if (i == 0) {
+            if (a.zero_state) return pl;  // no state copy
             pl.src = a.state_in + T.sbase + (long long)T.row0 * N;
             pl.dst = LY::kState;
             pl.bytes = (uint32_t)T.rows * N * 4;
@@ -834,7 +847,14 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         // Wait for the tile's bulk copies; the state tile goes to registers.
         const bool ok = mbar_wait_bounded(&bar, parity);
         float2 hs[2][G::kNC / 2];
-        load_state<N>(hs, L, T.rows);
+        if (a.zero_state) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int m = 0; m < G::kNC / 2; ++m) hs[rr][m] = make_float2(0.f, 0.f);
+        } else {
+            load_state<N>(hs, L, T.rows);
+        }
         // Every thread is done with the state tile and with the previous tile's
         // staged inputs; the vote makes a timeout a CTA-wide decision.
         if (__syncthreads_or(!ok)) {
@@ -867,6 +887,11 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         }
         parity ^= 1u;
         __syncthreads();  // staged inputs visible
+        if (!T.ok) {  // no valid pool slot: neither y nor the state is written
+            if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_SLOT);
+            t = tn;
+            continue;
+        }
 
         float *sl = (a.state != nullptr) ? a.state + T.sbase + (long long)T.row0 * N : nullptr;
 
@@ -928,6 +953,94 @@ __global__ void ssm_wait_timeout_kernel(uint32_t *status) {
     __syncwarp();
     const bool ok = mbar_wait_bounded(&bar, 0u);
     if (__any_sync(0xffffffffu, !ok) && threadIdx.x == 0 && status != nullptr) atomicOr(status, SSM_STATUS_TIMEOUT);
+}
+
+
+// Chunked prefill, the pass between the chunk passes: carry the state across a
+// prompt's chunks. Chunk c of sequence b, started from h = 0, left S_c in
+// ws[b * nch + c]; with lambda_c the product of its tokens' Abar,
+//     H_c = lambda_c H_{c-1} + S_c,   H_{-1} = the sequence's cached state,
+// which is the recurrence over the whole prompt regrouped by chunks. Each
+// chunk's slot of ws is overwritten with H_{c-1} (the state the chunk starts
+// from, for the output pass) and H_{nch-1} goes back to the cache.
+struct ScanArgs {
+    float *pool;            // cached states [nslots][H][P][N]
+    const int32_t *slot;    // pool slot of each sequence (nullptr: slot b)
+    int nslots;
+    float *ws;              // [batch * nch][H][P][N]
+    int32_t *vslot;         // [batch * nch]: chunk c of sequence b -> b * nch + c, or -1 for an invalid slot
+    const void *dt;         // [batch][T][H]
+    int in_bf16;
+    const float *A;
+    uint32_t *dev_status;
+    int H, nch, L;          // heads, chunks, tokens per chunk
+    long long PN;           // P * N
+};
+
+constexpr int kScanThreads = 256;
+constexpr int kScanPerThread = 4;  // state elements per thread
+
+__global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const ScanArgs a) {
+    extern __shared__ float lam[];  // [nch]
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float Ah = __ldg(a.A + h);
+    // lambda_c: one warp per chunk, a fixed product tree over the chunk's tokens
+    for (int c = warp; c < a.nch; c += kScanThreads / 32) {
+        float prod = 1.f;
+        for (int i = lane; i < a.L; i += 32) {
+            const long long t = (long long)b * a.nch * a.L + (long long)c * a.L + i;
+            const float dtv = a.in_bf16 ? ld1(static_cast<const __nv_bfloat16 *>(a.dt) + t * a.H + h)
+                                        : ld1(static_cast<const float *>(a.dt) + t * a.H + h);
+            prod = __fmul_rn(prod, ssm_decay(dtv, Ah));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) prod = __fmul_rn(prod, __shfl_xor_sync(~0u, prod, off));
+        if (lane == 0) lam[c] = prod;
+    }
+    int sidx = b;
+    bool ok = true;
+    if (a.slot != nullptr) {
+        sidx = __ldg(a.slot + b);
+        ok = sidx >= 0 && sidx < a.nslots;
+    }
+    if (!ok && blockIdx.x == 0 && h == 0 && tid == 0 && a.dev_status != nullptr)
+        atomicOr(a.dev_status, SSM_STATUS_BAD_SLOT);
+    if (a.vslot != nullptr && blockIdx.x == 0 && h == 0)
+        for (int c = tid; c < a.nch; c += kScanThreads) a.vslot[b * a.nch + c] = ok ? b * a.nch + c : -1;
+    __syncthreads();
+    const long long e0 = (long long)blockIdx.x * kScanThreads * kScanPerThread + tid;
+    float *cache = ok ? a.pool + ((long long)sidx * a.H + h) * a.PN : nullptr;
+    float Hs[kScanPerThread];
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) {
+        const long long e = e0 + (long long)k * kScanThreads;
+        Hs[k] = (ok && e < a.PN) ? cache[e] : 0.f;  // an invalid slot starts from h = 0
+    }
+    const long long cstride = (long long)a.H * a.PN;  // between consecutive chunks of one sequence
+    float *w = a.ws + ((long long)b * a.nch * a.H + h) * a.PN;
+    for (int c = 0; c < a.nch; ++c) {
+        const float l = lam[c];
+        float S[kScanPerThread];
+#pragma unroll
+        for (int k = 0; k < kScanPerThread; ++k) {
+            const long long e = e0 + (long long)k * kScanThreads;
+            S[k] = e < a.PN ? __ldcs(w + c * cstride + e) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kScanPerThread; ++k) {
+            const long long e = e0 + (long long)k * kScanThreads;
+            if (e < a.PN) w[c * cstride + e] = Hs[k];
+            Hs[k] = fmaf(l, Hs[k], S[k]);
+        }
+    }
+    if (ok) {
+#pragma unroll
+        for (int k = 0; k < kScanPerThread; ++k) {
+            const long long e = e0 + (long long)k * kScanThreads;
+            if (e < a.PN) cache[e] = Hs[k];
+        }
+    }
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -1054,10 +1167,15 @@ struct Call {
     const int32_t *accept_len;
     float *y;
     uint32_t *dev_status;
+    bool pool = false;              // `state` is a pool of nslots sequence states
+    const int32_t *slot = nullptr;  // pool slot of each sequence (nullptr: slot b for sequence b)
+    int nslots = 0;
+    bool zero_state = false;        // internal: every tile starts from h = 0, nothing is read
+    bool accept_all = false;        // internal: the replay block is replayed in full (no accept_len)
 };
 
-// Validate everything on the host, then launch.
-int run(const ssm_desc_t *d, const Call &c, void *stream) {
+// Validate everything on the host, then launch (with dry: validate only).
+int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     int rc = check_desc(d);
     if (rc != SSM_OK) return rc;
     const int F = c.flavour;
@@ -1073,15 +1191,20 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
     if (d->batch == 0) return SSM_OK;
 
     const void *st = F == kVerify ? static_cast<const void *>(c.state_in) : static_cast<const void *>(c.state);
-    if (st == nullptr || c.A == nullptr) return SSM_ERR_NULL;
+    if ((st == nullptr && !c.zero_state) || c.A == nullptr) return SSM_ERR_NULL;
+    if (c.pool) {
+        if (c.nslots < 1) return SSM_ERR_SHAPE;
+        if (c.slot == nullptr && c.nslots < d->batch) return SSM_ERR_SHAPE;
+        if (c.slot != nullptr && !aligned(c.slot, 4)) return SSM_ERR_ALIGN;
+    }
     if (verify_phase && (c.x == nullptr || c.B == nullptr || c.C == nullptr || c.dt == nullptr || c.D == nullptr ||
                          c.y == nullptr))
         return SSM_ERR_NULL;
-    if (replay && (c.xr == nullptr || c.Br == nullptr || c.dtr == nullptr || c.accept_len == nullptr))
+    if (replay && (c.xr == nullptr || c.Br == nullptr || c.dtr == nullptr || (c.accept_len == nullptr && !c.accept_all)))
         return SSM_ERR_NULL;
 
     const uintptr_t eb = d->in_dtype == SSM_BF16 ? 2 : 4;
-    if (!aligned(st, 16) || !aligned(c.A, 4)) return SSM_ERR_ALIGN;
+    if ((st != nullptr && !aligned(st, 16)) || !aligned(c.A, 4)) return SSM_ERR_ALIGN;
     if (verify_phase && (!aligned(c.x, eb) || !aligned(c.B, eb) || !aligned(c.C, eb) || !aligned(c.dt, eb) ||
                          !aligned(c.D, 4) || !aligned(c.y, 4)))
         return SSM_ERR_ALIGN;
@@ -1090,9 +1213,10 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
     if (c.dev_status != nullptr && !aligned(c.dev_status, 4)) return SSM_ERR_ALIGN;
 
     const int64_t B_ = d->batch, H = d->nheads, P = d->headdim, G = d->ngroups;
-    const int64_t state_bytes = B_ * H * P * N * 4;
+    const int64_t state_bytes = (c.pool ? (int64_t)c.nslots : B_) * H * P * N * 4;
     BufList bl;
-    bl.add(st, state_bytes, F != kVerify);
+    if (st != nullptr) bl.add(st, state_bytes, F != kVerify);
+    if (c.pool && c.slot != nullptr) bl.add(c.slot, B_ * 4, false);
     bl.add(c.A, H * 4, false);
     if (verify_phase) {
         const int64_t bk = B_ * d->ntok;
@@ -1117,10 +1241,14 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
     if (c.accept_len != nullptr) bl.add(c.accept_len, B_ * 4, false);
     if (c.dev_status != nullptr) bl.add(c.dev_status, 4, true);
     if (!bl.disjoint_writes()) return SSM_ERR_ALIAS;
+    if (dry) return SSM_OK;
 
     Args a;
-    a.state_in = static_cast<const float *>(st);
+    a.state_in = c.zero_state ? nullptr : static_cast<const float *>(st);
     a.state = F == kVerify ? nullptr : c.state;
+    a.slot = c.pool ? c.slot : nullptr;
+    a.nslots = c.pool ? c.nslots : 0;
+    a.zero_state = c.zero_state ? 1 : 0;
     const uintptr_t rowb = (uintptr_t)P * eb;
     a.ver.x = c.x;
     a.ver.B = c.B;
@@ -1161,6 +1289,166 @@ int run(const ssm_desc_t *d, const Call &c, void *stream) {
         g_last_cuda_error = (int)e;
         return SSM_ERR_CUDA;
     }
+    return SSM_OK;
+}
+
+
+// SM count of the current device (immutable; cached per device).
+int device_sms() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+constexpr int kMaxChunks = 4096;
+
+// Workspace of a chunked prefill with chunk length L: the chunk states, then
+// the chunks' slot map (16-byte aligned).
+int64_t prefill_ws_states(const ssm_desc_t *d, int L) {
+    return (int64_t)d->batch * (d->ntok / L) * d->nheads * d->headdim * d->dstate * 4;
+}
+int64_t prefill_ws_bytes(const ssm_desc_t *d, int L) {
+    return prefill_ws_states(d, L) + ((int64_t)d->batch * (d->ntok / L) * 4 + 15) / 16 * 16;
+}
+
+// Chunk length of a chunked prefill: the largest of 256, 128, 64, 32, 16
+// that divides the prompt into at least two chunks, fits the workspace and
+// gives one wave of tiles (four per SM); the smallest fitting one if none
+// reaches a wave. 0: the one-pass form (it fills the device by itself, or no
+// chunk length fits).
+int prefill_chunk_len(const ssm_desc_t *d, int64_t ws_bytes) {
+    const int T = d->ntok;
+    const int ROWS = rows_per_tile(d->dstate);
+    const int64_t ptiles = (d->headdim + ROWS - 1) / ROWS;
+    const int64_t base = (int64_t)d->batch * d->nheads * ptiles;
+    const int64_t wave = (int64_t)device_sms() * 4;
+    if (wave <= 0 || base >= wave) return 0;
+    int best = 0;
+    for (int L = 256; L >= 16; L >>= 1) {
+        if (T % L != 0 || T / L < 2 || T / L > kMaxChunks) continue;
+        if (ws_bytes >= 0 && prefill_ws_bytes(d, L) > ws_bytes) continue;
+        best = L;
+        if (base * (T / L) >= wave) break;
+    }
+    return best;
+}
+
+int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+            const void *dt, const float *A, const float *D, float *y, void *ws, int64_t ws_bytes,
+            uint32_t *dev_status, void *stream) {
+    int rc = check_desc(d);
+    if (rc != SSM_OK) return rc;
+    if (pool == nullptr) return SSM_ERR_NULL;
+    if (pool->reserved != 0 || ws_bytes < 0) return SSM_ERR_SHAPE;
+    if (d->batch == 0) return SSM_OK;
+    Call c{};
+    c.flavour = kVerifyCommit;  // every prompt token is kept: accept_len = nullptr means all
+    c.state = pool->states;
+    c.pool = true;
+    c.slot = pool->slot;
+    c.nslots = pool->nslots;
+    c.x = x; c.B = B; c.C = C; c.dt = dt;
+    c.A = A; c.D = D; c.y = y;
+    c.dev_status = dev_status;
+    rc = run(d, c, stream, true);
+    if (rc != SSM_OK) return rc;
+    const int L = prefill_chunk_len(d, ws == nullptr ? 0 : ws_bytes);
+    if (L == 0) return run(d, c, stream);
+
+    // Chunked: (1) every chunk from h = 0 -> ws; (2) carry across chunks;
+    // (3) y of every chunk from the state it starts from.
+    const int nch = d->ntok / L;
+    const int64_t H = d->nheads, P = d->headdim, N = d->dstate, G = d->ngroups, Bn = d->batch;
+    const int64_t need = prefill_ws_bytes(d, L);
+    if (!aligned(ws, 16)) return SSM_ERR_ALIGN;
+    const uintptr_t eb = d->in_dtype == SSM_BF16 ? 2 : 4;
+    const int64_t bt = Bn * d->ntok;
+    const Range w = range_of(ws, need);
+    const Range others[] = {range_of(pool->states, (int64_t)pool->nslots * H * P * N * 4),
+                            range_of(x, bt * H * P * eb), range_of(B, bt * G * N * eb), range_of(C, bt * G * N * eb),
+                            range_of(dt, bt * H * eb), range_of(A, H * 4), range_of(D, H * 4),
+                            range_of(y, bt * H * P * 4)};
+    for (const Range &o : others)
+        if (overlaps(w, o)) return SSM_ERR_ALIAS;
+    if (pool->slot != nullptr && overlaps(w, range_of(pool->slot, Bn * 4))) return SSM_ERR_ALIAS;
+    if (dev_status != nullptr && overlaps(w, range_of(dev_status, 4))) return SSM_ERR_ALIAS;
+
+    ssm_desc_t dv = *d;  // chunk c of sequence b is virtual sequence b * nch + c
+    dv.batch = (int32_t)(Bn * nch);
+    dv.ntok = L;
+    Call c1{};
+    c1.flavour = kCommit;
+    c1.state = static_cast<float *>(ws);
+    c1.zero_state = true;
+    c1.accept_all = true;
+    c1.xr = x; c1.Br = B; c1.dtr = dt;
+    c1.A = A;
+    c1.dev_status = dev_status;
+    rc = run(&dv, c1, stream);
+    if (rc != SSM_OK) return rc;
+
+    ScanArgs sa;
+    sa.pool = pool->states;
+    sa.slot = pool->slot;
+    sa.nslots = pool->nslots;
+    sa.ws = static_cast<float *>(ws);
+    int32_t *vslot = pool->slot != nullptr
+                         ? reinterpret_cast<int32_t *>(static_cast<char *>(ws) + prefill_ws_states(d, L))
+                         : nullptr;
+    sa.vslot = vslot;
+    sa.dt = dt;
+    sa.in_bf16 = d->in_dtype == SSM_BF16;
+    sa.A = A;
+    sa.dev_status = dev_status;
+    sa.H = (int)H;
+    sa.nch = nch;
+    sa.L = L;
+    sa.PN = P * N;
+    const dim3 grid((unsigned)((P * N + kScanThreads * kScanPerThread - 1) / (kScanThreads * kScanPerThread)),
+                    (unsigned)H, (unsigned)Bn);
+    ssm_chunk_scan_kernel<<<grid, kScanThreads, nch * sizeof(float), static_cast<cudaStream_t>(stream)>>>(sa);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return SSM_ERR_CUDA;
+    }
+
+    Call c3{};
+    c3.flavour = kVerify;
+    c3.state_in = static_cast<const float *>(ws);
+    if (vslot != nullptr) {  // chunks of sequences without a valid slot write no y
+        c3.pool = true;
+        c3.slot = vslot;
+        c3.nslots = dv.batch;
+    }
+    c3.x = x; c3.B = B; c3.C = C; c3.dt = dt;
+    c3.A = A; c3.D = D; c3.y = y;
+    c3.dev_status = dev_status;
+    return run(&dv, c3, stream);
+}
+
+Call pool_call(int flavour, const ssm_pool_t *pool) {
+    Call c{};
+    c.flavour = flavour;
+    c.pool = true;
+    if (pool != nullptr) {
+        c.state = pool->states;
+        c.state_in = pool->states;
+        c.slot = pool->slot;
+        c.nslots = pool->nslots;
+    }
+    return c;
+}
+
+int check_pool(const ssm_pool_t *pool) {
+    if (pool == nullptr) return SSM_ERR_NULL;
+    if (pool->reserved != 0) return SSM_ERR_SHAPE;
     return SSM_OK;
 }
 
@@ -1235,6 +1523,83 @@ int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B,
     c.A = A; c.D = D; c.y = y;
     c.dev_status = dev_status;
     return run(desc, c, stream);
+}
+
+int ssm_verify_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                    const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream) {
+    const int rc = check_pool(pool);
+    if (rc != SSM_OK) return rc;
+    Call c = pool_call(kVerify, pool);
+    c.x = x; c.B = B; c.C = C; c.dt = dt;
+    c.A = A; c.D = D; c.y = y;
+    c.dev_status = dev_status;
+    return run(desc, c, stream);
+}
+
+int ssm_commit_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *dt,
+                    const float *A, const int32_t *accept_len, uint32_t *dev_status, void *stream) {
+    const int rc = check_pool(pool);
+    if (rc != SSM_OK) return rc;
+    Call c = pool_call(kCommit, pool);
+    c.xr = x; c.Br = B; c.dtr = dt;
+    c.A = A;
+    c.accept_len = accept_len;
+    c.dev_status = dev_status;
+    return run(desc, c, stream);
+}
+
+int ssm_verify_commit_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B,
+                           const void *C, const void *dt, const float *A, const float *D, const int32_t *accept_len,
+                           float *y, uint32_t *dev_status, void *stream) {
+    const int rc = check_pool(pool);
+    if (rc != SSM_OK) return rc;
+    if (accept_len == nullptr && desc != nullptr && desc->batch > 0) return SSM_ERR_NULL;
+    Call c = pool_call(kVerifyCommit, pool);
+    c.x = x; c.B = B; c.C = C; c.dt = dt;
+    c.A = A; c.D = D; c.y = y;
+    c.accept_len = accept_len;
+    c.dev_status = dev_status;
+    return run(desc, c, stream);
+}
+
+int ssm_commit_verify_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, int32_t prev_ntok, const void *x_prev,
+                           const void *B_prev, const void *dt_prev, const int32_t *accept_len_prev, const void *x,
+                           const void *B, const void *C, const void *dt, const float *A, const float *D, float *y,
+                           uint32_t *dev_status, void *stream) {
+    const int rc = check_pool(pool);
+    if (rc != SSM_OK) return rc;
+    Call c = pool_call(kCommitVerify, pool);
+    c.rep_ntok = prev_ntok;
+    c.xr = x_prev; c.Br = B_prev; c.dtr = dt_prev;
+    c.accept_len = accept_len_prev;
+    c.x = x; c.B = B; c.C = C; c.dt = dt;
+    c.A = A; c.D = D; c.y = y;
+    c.dev_status = dev_status;
+    return run(desc, c, stream);
+}
+
+int ssm_step_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                  const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream) {
+    const int rc = check_pool(pool);
+    if (rc != SSM_OK) return rc;
+    if (desc != nullptr && desc->ntok != 1) return SSM_ERR_SHAPE;
+    Call c = pool_call(kVerifyCommit, pool);
+    c.x = x; c.B = B; c.C = C; c.dt = dt;
+    c.A = A; c.D = D; c.y = y;
+    c.dev_status = dev_status;
+    return run(desc, c, stream);
+}
+
+int64_t ssm_prefill_workspace_bytes(const ssm_desc_t *desc) {
+    if (check_desc(desc) != SSM_OK || desc->batch == 0) return 0;
+    const int L = prefill_chunk_len(desc, -1);
+    return L == 0 ? 0 : prefill_ws_bytes(desc, L);
+}
+
+int ssm_prefill(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                const void *dt, const float *A, const float *D, float *y, void *workspace, int64_t workspace_bytes,
+                uint32_t *dev_status, void *stream) {
+    return prefill(desc, pool, x, B, C, dt, A, D, y, workspace, workspace_bytes, dev_status, stream);
 }
 
 int ssm_selftest_wait_timeout(uint32_t *dev_status, void *stream) {

@@ -32,18 +32,25 @@ SSM_ERR_CUDA = 6
 SSM_STATUS_BAD_ACCEPT_LEN = 1
 SSM_STATUS_TIMEOUT = 2
 SSM_STATUS_BAD_TOKEN = 4
+SSM_STATUS_BAD_SLOT = 8
 SSM_ACCEPT_MAX_NTOK = 32
 SSM_ACCEPT_MAX_VOCAB = 1 << 28
 
 EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
-           "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample", "ssm_strerror",
-           "ssm_last_cuda_error", "ssm_version")
+           "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool", "ssm_step_pool",
+           "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_selftest_wait_timeout", "ssm_accept_greedy",
+           "ssm_accept_sample", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
 
 
 class SsmDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
                 ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("ntok", ctypes.c_int32),
                 ("in_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("states", ctypes.c_void_p), ("slot", ctypes.c_void_p), ("nslots", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class AcceptDesc(ctypes.Structure):
@@ -80,9 +87,19 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     ap = ctypes.POINTER(AcceptDesc)
     lib.ssm_accept_greedy.argtypes = [ap] + [vp] * 6
     lib.ssm_accept_sample.argtypes = [ap] + [vp] * 8
+    pp = ctypes.POINTER(PoolDesc)
+    lib.ssm_verify_pool.argtypes = [dp, pp] + [vp] * 10
+    lib.ssm_commit_pool.argtypes = [dp, pp] + [vp] * 8
+    lib.ssm_verify_commit_pool.argtypes = [dp, pp] + [vp] * 11
+    lib.ssm_commit_verify_pool.argtypes = [dp, pp, ctypes.c_int32] + [vp] * 13
+    lib.ssm_step_pool.argtypes = [dp, pp] + [vp] * 10
+    lib.ssm_prefill.argtypes = [dp, pp] + [vp] * 8 + [ctypes.c_int64, vp, vp]
+    lib.ssm_prefill_workspace_bytes.argtypes = [dp]
+    lib.ssm_prefill_workspace_bytes.restype = ctypes.c_int64
     for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
-              "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample", "ssm_last_cuda_error",
-              "ssm_version"):
+              "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool",
+              "ssm_step_pool", "ssm_prefill", "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample",
+              "ssm_last_cuda_error", "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
     lib.ssm_strerror.restype = ctypes.c_char_p
@@ -127,7 +144,9 @@ def make_desc(state_shape, x_shape, B_shape, in_dtype: int) -> SsmDesc:
     return SsmDesc(bsz, H, P, N, G, K, in_dtype, 0)
 
 
-def _validate(state, x, B, C, dt, A, D, accept_len, y):
+def _validate(state, x, B, C, dt, A, D, accept_len, y, pooled=False):
+    """Check the tensors of one call; with `pooled`, `state` is a pool
+    [nslots][H][P][N] and the batch comes from x."""
     tensors = {"state": state, "x": x, "B": B, "dt": dt, "A": A}
     for k, v in (("C", C), ("D", D), ("accept_len", accept_len), ("y", y)):
         if v is not None:
@@ -140,7 +159,8 @@ def _validate(state, x, B, C, dt, A, D, accept_len, y):
             raise ValueError(f"{k} must be contiguous")
     if state.dtype != torch.float32 or state.dim() != 4:
         raise ValueError("state must be float32 [batch][H][P][N]")
-    bsz, H, P, N = state.shape
+    _, H, P, N = state.shape
+    bsz = x.shape[0] if pooled else state.shape[0]
     if x.dim() != 4 or x.shape[0] != bsz or x.shape[2] != H or x.shape[3] != P:
         raise ValueError(f"x must be [batch][K][H][P] = [{bsz}][K][{H}][{P}], got {tuple(x.shape)}")
     K = x.shape[1]
@@ -161,7 +181,7 @@ def _validate(state, x, B, C, dt, A, D, accept_len, y):
         raise ValueError("accept_len must be int32 [batch]")
     if y is not None and (y.dtype != torch.float32 or tuple(y.shape) != (bsz, K, H, P)):
         raise ValueError("y must be float32 [batch][K][H][P]")
-    return make_desc(state.shape, x.shape, B.shape, _in_dtype(x)), G
+    return SsmDesc(bsz, H, P, N, G, K, _in_dtype(x), 0), G
 
 
 def _new_y(state, x):
@@ -306,3 +326,106 @@ def accept_sample(target_logits, draft_logits, draft_tokens, uniform, accept_len
                                             _ptr(draft_tokens), _ptr(uniform), _ptr(accept_len), _ptr(next_token),
                                             _ptr(dev_status), _stream(stream)))
     return accept_len, next_token
+
+
+# ----------------------------------------------------------------------------- state pool and prefill
+
+def _pool(states: torch.Tensor, slot: Optional[torch.Tensor], bsz: int):
+    """The C pool descriptor: `states` [nslots][H][P][N] fp32 CUDA, `slot`
+    int32 [batch] CUDA (None: sequence b uses slot b)."""
+    if not states.is_cuda or states.dtype != torch.float32 or states.dim() != 4 or not states.is_contiguous():
+        raise ValueError("pool states must be a contiguous float32 CUDA tensor [nslots][H][P][N]")
+    if slot is not None:
+        if not slot.is_cuda or slot.device != states.device or slot.dtype != torch.int32 or \
+                tuple(slot.shape) != (bsz,) or not slot.is_contiguous():
+            raise ValueError(f"slot must be a contiguous int32 CUDA tensor [{bsz}] on {states.device}")
+    return PoolDesc(states.data_ptr(), None if slot is None else slot.data_ptr(), states.shape[0], 0)
+
+
+def verify_pool(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
+    """verify on the pool slots `slot` of `states` (read only)."""
+    y = _new_y(states, x) if y is None else y
+    desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
+    pool = _pool(states, slot, x.shape[0])
+    _check(load_library().ssm_verify_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
+                                          _ptr(dt), _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def commit_pool(states, slot, x, B, dt, A, accept_len, dev_status=None, stream=None) -> None:
+    """commit into the pool slots."""
+    desc, _ = _validate(states, x, B, None, dt, A, None, accept_len, None, pooled=True)
+    pool = _pool(states, slot, x.shape[0])
+    _check(load_library().ssm_commit_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(dt),
+                                          _ptr(A), _ptr(accept_len), _ptr(dev_status), _stream(stream)))
+
+
+def verify_commit_pool(states, slot, x, B, C, dt, A, D, accept_len, y=None, dev_status=None,
+                       stream=None) -> torch.Tensor:
+    """verify_commit on the pool slots."""
+    y = _new_y(states, x) if y is None else y
+    desc, _ = _validate(states, x, B, C, dt, A, D, accept_len, y, pooled=True)
+    pool = _pool(states, slot, x.shape[0])
+    _check(load_library().ssm_verify_commit_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
+                                                 _ptr(dt), _ptr(A), _ptr(D), _ptr(accept_len), _ptr(y),
+                                                 _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def commit_verify_pool(states, slot, x_prev, B_prev, dt_prev, accept_len_prev, x, B, C, dt, A, D, y=None,
+                       dev_status=None, stream=None) -> torch.Tensor:
+    """commit_verify on the pool slots."""
+    y = _new_y(states, x) if y is None else y
+    desc, G = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
+    bsz = x.shape[0]
+    _, H, P, N = states.shape
+    kp = x_prev.shape[1]
+    for k, v, shape in (("x_prev", x_prev, (bsz, kp, H, P)), ("B_prev", B_prev, (bsz, kp, G, N)),
+                        ("dt_prev", dt_prev, (bsz, kp, H))):
+        if tuple(v.shape) != shape or v.dtype != x.dtype or not v.is_cuda or not v.is_contiguous():
+            raise ValueError(f"{k} must be a contiguous {x.dtype} CUDA tensor {list(shape)}")
+    if accept_len_prev.dtype != torch.int32 or tuple(accept_len_prev.shape) != (bsz,) or not accept_len_prev.is_cuda:
+        raise ValueError("accept_len_prev must be int32 [batch] on the GPU")
+    pool = _pool(states, slot, bsz)
+    _check(load_library().ssm_commit_verify_pool(ctypes.byref(desc), ctypes.byref(pool), kp, _ptr(x_prev),
+                                                 _ptr(B_prev), _ptr(dt_prev), _ptr(accept_len_prev), _ptr(x), _ptr(B),
+                                                 _ptr(C), _ptr(dt), _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status),
+                                                 _stream(stream)))
+    return y
+
+
+def step_pool(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
+    """step (K = 1) on the pool slots."""
+    y = _new_y(states, x) if y is None else y
+    desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
+    pool = _pool(states, slot, x.shape[0])
+    _check(load_library().ssm_step_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
+                                        _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def prefill_workspace_bytes(states, x, B, C, dt, A, D) -> int:
+    """Workspace (bytes) that prefill would use for these shapes (0: none)."""
+    desc, _ = _validate(states, x, B, C, dt, A, D, None, None, pooled=True)
+    return int(load_library().ssm_prefill_workspace_bytes(ctypes.byref(desc)))
+
+
+def prefill(states, slot, x, B, C, dt, A, D, y=None, workspace=None, dev_status=None,
+            stream=None) -> torch.Tensor:
+    """Run the prompt x/B/C/dt [batch][T]... from each sequence's cached
+    state (pool slot), write y for every prompt token and leave the final
+    state in the slot. `workspace` (a CUDA tensor) enables the chunked form;
+    by default it is allocated here at the size the library asks for."""
+    y = _new_y(states, x) if y is None else y
+    desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
+    pool = _pool(states, slot, x.shape[0])
+    lib = load_library()
+    if workspace is None:
+        nbytes = int(lib.ssm_prefill_workspace_bytes(ctypes.byref(desc)))
+        workspace = torch.empty(max(nbytes, 0) // 4, dtype=torch.float32, device=states.device) if nbytes > 0 else None
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.ssm_prefill(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
+                           _ptr(D), _ptr(y), _ptr(workspace), wbytes, _ptr(dev_status), _stream(stream)))
+    return y

@@ -1,0 +1,196 @@
+"""State-pool entry points and prefill on the GPU, through the C ABI.
+
+Pool variants are the plain entry points with the state reached through a
+slot map: on the same data they must give the plain results bit for bit and
+leave every other slot untouched. Prefill is the recurrence over a whole
+prompt from the cached state: it is compared with the fp64 oracle (every
+token accepted), in its one-pass and its chunked form."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssm_recurrence_verify_b300 as ssm
+from gpu_helpers import RTOL_STATE, np64, rel_err, y_tol
+from ssm_recurrence_verify_b300 import ssmverify as sv
+from ssm_recurrence_verify_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(batch, H, P, N, G, K, dtype, seed, rnd=0):
+    wl = synth.custom_workload(batch, H, P, N, G, K, dtype, seed=seed)
+    p = synth.draw_params(wl)
+    t = synth.draw_tokens(wl, rnd)
+    return wl, p, t
+
+
+def _dev(d, dev):
+    return {k: v.to(dev) for k, v in d.items()}
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_pool_variants_equal_plain_calls(cuda_device, dtype):
+    dev = cuda_device
+    batch, H, P, N, G, K = 4, 4, 64, 128, 2, 5
+    wl, p, t = _inputs(batch, H, P, N, G, K, dtype, seed=301)
+    nslots = 7
+    slot = torch.tensor([5, 0, 3, 6], dtype=torch.int32)
+    pool0 = torch.randn(nslots, H, P, N, generator=torch.Generator().manual_seed(3)) * 0.1
+    pool0[slot.long()] = p["state0"]
+    td = _dev(t, dev)
+    A, D = p["A"].to(dev), p["D"].to(dev)
+    acc = synth.draw_accept_len(wl, 0).to(dev)
+    sl = slot.to(dev)
+    others = [i for i in range(nslots) if i not in slot.tolist()]
+
+    def fresh():
+        return pool0.clone().to(dev), p["state0"].clone().to(dev)
+
+    # verify
+    pool, st = fresh()
+    y_p = ssm.verify_pool(pool, sl, td["x"], td["B"], td["C"], td["dt"], A, D)
+    y_s = ssm.verify(st, td["x"], td["B"], td["C"], td["dt"], A, D)
+    torch.cuda.synchronize()
+    assert torch.equal(y_p, y_s) and torch.equal(pool.cpu(), pool0)
+    # verify_commit
+    pool, st = fresh()
+    y_p = ssm.verify_commit_pool(pool, sl, td["x"], td["B"], td["C"], td["dt"], A, D, acc)
+    y_s = ssm.verify_commit(st, td["x"], td["B"], td["C"], td["dt"], A, D, acc)
+    torch.cuda.synchronize()
+    assert torch.equal(y_p, y_s) and torch.equal(pool[sl.long()], st)
+    assert torch.equal(pool.cpu()[others], pool0[others])
+    # commit
+    pool, st = fresh()
+    ssm.commit_pool(pool, sl, td["x"], td["B"], td["dt"], A, acc)
+    ssm.commit(st, td["x"], td["B"], td["dt"], A, acc)
+    torch.cuda.synchronize()
+    assert torch.equal(pool[sl.long()], st) and torch.equal(pool.cpu()[others], pool0[others])
+    # commit_verify (previous block = this round's, new block = the next round's)
+    t2 = _dev(synth.draw_tokens(wl, 1), dev)
+    pool, st = fresh()
+    y_p = ssm.commit_verify_pool(pool, sl, td["x"], td["B"], td["dt"], acc, t2["x"], t2["B"], t2["C"], t2["dt"], A, D)
+    y_s = ssm.commit_verify(st, td["x"], td["B"], td["dt"], acc, t2["x"], t2["B"], t2["C"], t2["dt"], A, D)
+    torch.cuda.synchronize()
+    assert torch.equal(y_p, y_s) and torch.equal(pool[sl.long()], st)
+    assert torch.equal(pool.cpu()[others], pool0[others])
+    # step, and the identity map (slot None: sequence b uses slot b)
+    w1, p1, t1 = _inputs(batch, H, P, N, G, 1, dtype, seed=302)
+    t1 = _dev(t1, dev)
+    pool, st = fresh()
+    y_p = ssm.step_pool(pool, sl, t1["x"], t1["B"], t1["C"], t1["dt"], A, D)
+    y_s = ssm.step(st, t1["x"], t1["B"], t1["C"], t1["dt"], A, D)
+    torch.cuda.synchronize()
+    assert torch.equal(y_p, y_s) and torch.equal(pool[sl.long()], st)
+    pool = p["state0"].clone().to(dev)
+    st = p["state0"].clone().to(dev)
+    y_p = ssm.verify_commit_pool(pool, None, td["x"], td["B"], td["C"], td["dt"], A, D, acc)
+    y_s = ssm.verify_commit(st, td["x"], td["B"], td["C"], td["dt"], A, D, acc)
+    torch.cuda.synchronize()
+    assert torch.equal(y_p, y_s) and torch.equal(pool, st)
+
+
+@pytest.mark.parametrize("fn,K", [("verify_commit", 3), ("prefill", 3), ("prefill", 64)])
+def test_bad_slots_write_nothing(cuda_device, fn, K):
+    """Sequences whose slot is outside [0, nslots): status bit set, their y
+    and every slot no valid sequence maps to untouched (prefill with K = 64
+    takes the chunked form)."""
+    dev = cuda_device
+    batch, H, P, N, G = 4, 2, 32, 64, 1
+    wl, p, t = _inputs(batch, H, P, N, G, K, synth.F32, seed=303)
+    td = _dev(t, dev)
+    A, D = p["A"].to(dev), p["D"].to(dev)
+    acc = torch.full((batch,), K, dtype=torch.int32, device=dev)
+    pool0 = p["state0"].clone()
+    slot = torch.tensor([1, 4, -1, 2], dtype=torch.int32, device=dev)  # nslots = 4: 4 and -1 are invalid
+    pool = pool0.clone().to(dev)
+    y = torch.full((batch, K, H, P), 7.0, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if fn == "verify_commit":
+        ssm.verify_commit_pool(pool, slot, td["x"], td["B"], td["C"], td["dt"], A, D, acc, y=y, dev_status=st)
+    else:
+        if K == 64:
+            assert ssm.prefill_workspace_bytes(pool, td["x"], td["B"], td["C"], td["dt"], A, D) > 0
+        ssm.prefill(pool, slot, td["x"], td["B"], td["C"], td["dt"], A, D, y=y, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & sv.SSM_STATUS_BAD_SLOT
+    assert torch.equal(pool[0].cpu(), pool0[0]) and torch.equal(pool[3].cpu(), pool0[3])  # no sequence maps here
+    assert (y[1] == 7.0).all() and (y[2] == 7.0).all()  # bad slots: y untouched
+    assert not (y[0] == 7.0).any() and not (y[3] == 7.0).any()
+    # the valid sequences match the plain call on their own states
+    ref = oracle.verify_commit(pool0[[1, 2]], t["x"][[0, 3]], t["B"][[0, 3]], t["C"][[0, 3]], t["dt"][[0, 3]],
+                               p["A"], p["D"], None)
+    assert rel_err(np64(y[[0, 3]]), ref["y"]) <= 1e-4
+    assert rel_err(np64(pool[[1, 2]]), ref["state"]) <= 1e-4
+
+
+def _prefill_case(dev, batch, H, P, N, G, T, dtype, seed, chunked=True):
+    wl, p, t = _inputs(batch, H, P, N, G, T, dtype, seed=seed)
+    nslots = batch + 2
+    slot = torch.randperm(nslots, generator=torch.Generator().manual_seed(seed))[:batch].to(torch.int32)
+    pool0 = torch.zeros(nslots, H, P, N)
+    pool0[slot.long()] = p["state0"]  # a continuing prompt: start from a nonzero cached state
+    pool = pool0.to(dev)
+    td = _dev(t, dev)
+    A, D = p["A"].to(dev), p["D"].to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = None if chunked else torch.empty(0, device=dev)
+    y = ssm.prefill(pool, slot.to(dev), td["x"], td["B"], td["C"], td["dt"], A, D, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.verify_commit(p["state0"], t["x"], t["B"], t["C"], t["dt"], p["A"], p["D"], None)
+    ey = rel_err(np64(y), ref["y"])
+    es = rel_err(np64(pool[slot.long().to(dev)]), ref["state"])
+    assert ey <= y_tol(wl.torch_in_dtype), (T, dtype, ey)
+    assert es <= RTOL_STATE, (T, dtype, es)
+    untouched = [i for i in range(nslots) if i not in slot.tolist()]
+    assert torch.equal(pool.cpu()[untouched], pool0[untouched])
+    return y, pool
+
+
+@pytest.mark.parametrize("T", [1, 8, 40, 64, 96, 256, 1024])
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_prefill_matches_oracle(cuda_device, T, dtype):
+    _prefill_case(cuda_device, 2, 4, 64, 128, 2, T, dtype, seed=400 + T)
+
+
+def test_prefill_chunked_and_one_pass_agree(cuda_device):
+    """The chunked regrouping and the plain recurrence agree to rounding, and
+    the small shape really does take the chunked form."""
+    dev = cuda_device
+    args = dict(batch=1, H=4, P=64, N=128, G=2, T=512, dtype=synth.BF16, seed=451)
+    pool = torch.zeros(1, 4, 64, 128, device=dev)
+    x = torch.zeros(1, 512, 4, 64, dtype=torch.bfloat16, device=dev)
+    Bc = torch.zeros(1, 512, 2, 128, dtype=torch.bfloat16, device=dev)
+    dt = torch.zeros(1, 512, 4, dtype=torch.bfloat16, device=dev)
+    AD = torch.zeros(4, device=dev)
+    assert ssm.prefill_workspace_bytes(pool, x, Bc, Bc, dt, AD, AD) > 0
+    y1, s1 = _prefill_case(dev, chunked=True, **args)
+    y2, s2 = _prefill_case(dev, chunked=False, **args)
+    assert rel_err(np64(y1), np64(y2)) <= 1e-4 and rel_err(np64(s1), np64(s2)) <= 1e-4
+
+
+def test_prefill_llama_layer_shape(cuda_device):
+    """A Llama-3-8B-shaped layer (H 32, P 128, N 128, G 8), one 2048-token prompt."""
+    _prefill_case(cuda_device, 1, 32, 128, 128, 8, 2048, synth.BF16, seed=461)
+
+
+def test_prefill_then_speculative_round(cuda_device):
+    """Prefill a prompt, then verify + commit K drafts from the cached state:
+    the same as the oracle over the prompt followed by the drafts."""
+    dev = cuda_device
+    batch, H, P, N, G, T, K = 2, 4, 64, 64, 2, 256, 6
+    wl, p, t = _inputs(batch, H, P, N, G, T, synth.F32, seed=471)
+    w2 = synth.custom_workload(batch, H, P, N, G, K, synth.F32, seed=472)
+    t2 = synth.draw_tokens(w2, 0)
+    acc = synth.draw_accept_len(w2, 0)
+    pool = torch.zeros(batch, H, P, N, device=dev)
+    td, t2d = _dev(t, dev), _dev(t2, dev)
+    A, D = p["A"].to(dev), p["D"].to(dev)
+    ssm.prefill(pool, None, td["x"], td["B"], td["C"], td["dt"], A, D)
+    y = ssm.verify_commit_pool(pool, None, t2d["x"], t2d["B"], t2d["C"], t2d["dt"], A, D, acc.to(dev))
+    torch.cuda.synchronize()
+    zero = torch.zeros(batch, H, P, N)
+    r1 = oracle.verify_commit(zero, t["x"], t["B"], t["C"], t["dt"], p["A"], p["D"], None)
+    r2 = oracle.verify_commit(r1["state"], t2["x"], t2["B"], t2["C"], t2["dt"], p["A"], p["D"], acc)
+    assert rel_err(np64(y), r2["y"]) <= 1e-4 and rel_err(np64(pool), r2["state"]) <= 1e-4
