@@ -88,11 +88,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_accept_greedy.argtypes = [ap] + [vp] * 6
     lib.ssm_accept_sample.argtypes = [ap] + [vp] * 8
     pp = ctypes.POINTER(PoolDesc)
-    lib.ssm_verify_pool.argtypes = [dp, pp] + [vp] * 10
-    lib.ssm_commit_pool.argtypes = [dp, pp] + [vp] * 8
-    lib.ssm_verify_commit_pool.argtypes = [dp, pp] + [vp] * 11
+    lib.ssm_verify_pool.argtypes = [dp, pp] + [vp] * 9
+    lib.ssm_commit_pool.argtypes = [dp, pp] + [vp] * 7
+    lib.ssm_verify_commit_pool.argtypes = [dp, pp] + [vp] * 10
     lib.ssm_commit_verify_pool.argtypes = [dp, pp, ctypes.c_int32] + [vp] * 13
-    lib.ssm_step_pool.argtypes = [dp, pp] + [vp] * 10
+    lib.ssm_step_pool.argtypes = [dp, pp] + [vp] * 9
     lib.ssm_prefill.argtypes = [dp, pp] + [vp] * 8 + [ctypes.c_int64, vp, vp]
     lib.ssm_prefill_workspace_bytes.argtypes = [dp]
     lib.ssm_prefill_workspace_bytes.restype = ctypes.c_int64

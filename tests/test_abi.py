@@ -312,3 +312,17 @@ def test_accept_shim_checks_shapes():
     t = torch.zeros(2, 4, 10)
     with pytest.raises(ValueError, match="CUDA tensor"):
         sv.accept_greedy(t, torch.zeros(2, 3, dtype=torch.int32))
+
+
+def _arity(name):
+    """Parameter count of a header declaration."""
+    txt = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)", txt)
+    return len([a for a in m.group(1).split(",") if a.strip()])
+
+
+def test_binding_arities_match_header(lib):
+    for name in sv.EXPORTS:
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is not None:
+            assert len(argtypes) == _arity(name), name
