@@ -67,11 +67,19 @@ enum Flavour : int {
     kCommitVerify = 3,  // replay phase, h_j written, then the verify phase from h_j
 };
 
+// Option bits OR-ed into a flavour: the state is reached through a slot map
+// (a pool), and every tile starts from h = 0 without reading a state.
+constexpr int kPoolBit = 8;
+constexpr int kZeroBit = 16;
+
 template <int F>
 struct Flav {
-    static constexpr bool kReplay = F == kCommit || F == kCommitVerify;
-    static constexpr bool kVerifyPhase = F != kCommit;
-    static constexpr bool kWriteInVerify = F == kVerifyCommit;
+    static constexpr int kBase = F & 7;
+    static constexpr bool kReplay = kBase == kCommit || kBase == kCommitVerify;
+    static constexpr bool kVerifyPhase = kBase != kCommit;
+    static constexpr bool kWriteInVerify = kBase == kVerifyCommit;
+    static constexpr bool kPool = (F & kPoolBit) != 0;
+    static constexpr bool kZero = (F & kZeroBit) != 0;
 };
 
 // Per-N geometry. A band is 16 rows (one mma M block); WPB warps share a
@@ -142,9 +150,8 @@ struct Block {
 struct Args {
     const float *state_in;  // state read by the tile loads
     float *state;           // state written (nullptr for verify)
-    const int32_t *slot;    // pool slot of each sequence (nullptr: sequence b uses slot b)
-    int nslots;             // slots in the pool (with slot != nullptr)
-    int zero_state;         // every tile starts from h = 0 (no state is read)
+    const int32_t *slot;    // pool flavours: slot of each sequence (nullptr: sequence b uses slot b)
+    int nslots;             // pool flavours: slots in the pool
     Block ver;              // verify block: y for every token
     Block rep;              // replay block: advanced over its accepted prefix
     const float *A, *D;
@@ -355,6 +362,7 @@ struct Tile {
     bool ok;               // the sequence's pool slot is valid (else nothing is written)
 };
 
+template <bool POOL>
 __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, int N) {
     Tile T;
     const uint32_t tt = (uint32_t)t;  // the host keeps the tile count below 2^31
@@ -367,7 +375,7 @@ __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, in
     T.rows = min(kRows, a.P - T.row0);
     long long sb = T.b;
     T.ok = true;
-    if (a.slot != nullptr) {
+    if (POOL && a.slot != nullptr) {
         const int s = __ldg(a.slot + T.b);
         T.ok = s >= 0 && s < a.nslots;
         sb = T.ok ? s : 0;  // an invalid slot reads slot 0 (in bounds) and writes nothing
@@ -697,7 +705,7 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
 // an invalid j: nothing to replay, nothing to write).
 template <int F>
 __device__ __forceinline__ long long next_work(const Args &a, long long t) {
-    if constexpr (F == kCommit) {
+    if constexpr (Flav<F>::kBase == kCommit) {
         if (a.accept_len == nullptr) return t;  // every token of every sequence
         const long long per_b = (long long)a.H * a.ptiles;
         for (; t < a.ntiles; t += gridDim.x) {
@@ -762,16 +770,16 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
     auto plan = [&](long long tt, int buf) {
         Plan pl{nullptr, 0u, 0u, 0u};
         if (tt >= a.ntiles) return pl;
-        const Tile T = decode(a, tt, ROWS, N);
+        const Tile T = decode<FL::kPool>(a, tt, ROWS, N);
         const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.b, a.rep.K), kTC) : 0;
         const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
         const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
-        pl.total = (a.zero_state ? 0u : (uint32_t)T.rows * N * 4) + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
+        pl.total = (FL::kZero ? 0u : (uint32_t)T.rows * N * 4) + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
         const int ncopy = 1 + 2 * tcR + 3 * tcV;
         const int i = warp + 4 * lane;
         if (i >= ncopy) return pl;
         if (i == 0) {
-            if (a.zero_state) return pl;  // no state copy
+            if (FL::kZero) return pl;  // no state copy
             pl.src = a.state_in + T.sbase + (long long)T.row0 * N;
             pl.dst = LY::kState;
             pl.bytes = (uint32_t)T.rows * N * 4;
@@ -822,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
     auto load_in = [&](long long tt) {
         TileIn in{0.f, 0.f, 0, -1, {0.f, 0.f}, {0.f, 0.f}};
         if (tt >= a.ntiles) return in;
-        const Tile T = decode(a, tt, ROWS, N);
+        const Tile T = decode<FL::kPool>(a, tt, ROWS, N);
         in.Ah = __ldg(a.A + T.h);
         if (FL::kVerifyPhase) in.Dh = __ldg(a.D + T.h);
         if (FL::kReplay) in.jr = accepted(a, T.b, a.rep.K);
@@ -835,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
 
     uint32_t parity = 0;  // mbarrier phase; raw buffer of the current tile = parity
     while (t < a.ntiles) {
-        const Tile T = decode(a, t, ROWS, N);
+        const Tile T = decode<FL::kPool>(a, t, ROWS, N);
         const float Ah = cur.Ah, Dh = cur.Dh;
         const int jr = cur.jr, jw = cur.jw;
         const int tcR0 = min(jr, kTC), tcV0 = FL::kVerifyPhase ? min(a.ver.K, kTC) : 0;
@@ -847,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         // Wait for the tile's bulk copies; the state tile goes to registers.
         const bool ok = mbar_wait_bounded(&bar, parity);
         float2 hs[2][G::kNC / 2];
-        if (a.zero_state) {
+        if constexpr (FL::kZero) {
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
@@ -887,10 +895,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         }
         parity ^= 1u;
         __syncthreads();  // staged inputs visible
-        if (!T.ok) {  // no valid pool slot: neither y nor the state is written
-            if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_SLOT);
-            t = tn;
-            continue;
+        if constexpr (FL::kPool) {
+            if (!T.ok) {  // no valid pool slot: neither y nor the state is written
+                if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_SLOT);
+                t = tn;
+                continue;
+            }
         }
 
         float *sl = (a.state != nullptr) ? a.state + T.sbase + (long long)T.row0 * N : nullptr;
@@ -1248,7 +1258,6 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     a.state = F == kVerify ? nullptr : c.state;
     a.slot = c.pool ? c.slot : nullptr;
     a.nslots = c.pool ? c.nslots : 0;
-    a.zero_state = c.zero_state ? 1 : 0;
     const uintptr_t rowb = (uintptr_t)P * eb;
     a.ver.x = c.x;
     a.ver.B = c.B;
@@ -1279,11 +1288,18 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (F) {
+    const int FX = F | (c.pool ? kPoolBit : 0) | (c.zero_state ? kZeroBit : 0);
+    switch (FX) {
         case kVerify: e = launch_flavour<kVerify>(d->in_dtype, N, a, s); break;
         case kCommit: e = launch_flavour<kCommit>(d->in_dtype, N, a, s); break;
         case kCommitVerify: e = launch_flavour<kCommitVerify>(d->in_dtype, N, a, s); break;
-        default: e = launch_flavour<kVerifyCommit>(d->in_dtype, N, a, s); break;
+        case kVerifyCommit: e = launch_flavour<kVerifyCommit>(d->in_dtype, N, a, s); break;
+        case kVerify | kPoolBit: e = launch_flavour<kVerify | kPoolBit>(d->in_dtype, N, a, s); break;
+        case kCommit | kPoolBit: e = launch_flavour<kCommit | kPoolBit>(d->in_dtype, N, a, s); break;
+        case kCommitVerify | kPoolBit: e = launch_flavour<kCommitVerify | kPoolBit>(d->in_dtype, N, a, s); break;
+        case kVerifyCommit | kPoolBit: e = launch_flavour<kVerifyCommit | kPoolBit>(d->in_dtype, N, a, s); break;
+        case kCommit | kZeroBit: e = launch_flavour<kCommit | kZeroBit>(d->in_dtype, N, a, s); break;
+        default: return SSM_ERR_UNSUPPORTED;  // no kernel for this combination
     }
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
