@@ -988,7 +988,12 @@ struct ScanArgs {
 };
 
 constexpr int kScanThreads = 256;
-constexpr int kScanPerThread = 4;  // state elements per thread
+constexpr int kScanPerThread = 4;  // state elements per thread: one 16-byte vector
+constexpr int kScanAhead = 8;      // chunks whose loads are issued before the carry chain consumes them
+
+__device__ __forceinline__ float4 fma4(float l, float4 h, float4 s) {
+    return make_float4(fmaf(l, h.x, s.x), fmaf(l, h.y, s.y), fmaf(l, h.z, s.z), fmaf(l, h.w, s.w));
+}
 
 __global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const ScanArgs a) {
     extern __shared__ float lam[];  // [nch]
@@ -1019,38 +1024,26 @@ __global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const Scan
     if (a.vslot != nullptr && blockIdx.x == 0 && h == 0)
         for (int c = tid; c < a.nch; c += kScanThreads) a.vslot[b * a.nch + c] = ok ? b * a.nch + c : -1;
     __syncthreads();
-    const long long e0 = (long long)blockIdx.x * kScanThreads * kScanPerThread + tid;
-    float *cache = ok ? a.pool + ((long long)sidx * a.H + h) * a.PN : nullptr;
-    float Hs[kScanPerThread];
+    const long long e = ((long long)blockIdx.x * kScanThreads + tid) * kScanPerThread;  // P * N % 4 == 0
+    if (e >= a.PN) return;
+    float4 *cache = ok ? reinterpret_cast<float4 *>(a.pool + ((long long)sidx * a.H + h) * a.PN + e) : nullptr;
+    float4 H = ok ? *cache : make_float4(0.f, 0.f, 0.f, 0.f);  // an invalid slot starts from h = 0
+    const long long cstride = (long long)a.H * a.PN / kScanPerThread;  // chunk to chunk, in vectors
+    float4 *w = reinterpret_cast<float4 *>(a.ws + ((long long)b * a.nch * a.H + h) * a.PN + e);
+    for (int c0 = 0; c0 < a.nch; c0 += kScanAhead) {
+        float4 S[kScanAhead];
 #pragma unroll
-    for (int k = 0; k < kScanPerThread; ++k) {
-        const long long e = e0 + (long long)k * kScanThreads;
-        Hs[k] = (ok && e < a.PN) ? cache[e] : 0.f;  // an invalid slot starts from h = 0
-    }
-    const long long cstride = (long long)a.H * a.PN;  // between consecutive chunks of one sequence
-    float *w = a.ws + ((long long)b * a.nch * a.H + h) * a.PN;
-    for (int c = 0; c < a.nch; ++c) {
-        const float l = lam[c];
-        float S[kScanPerThread];
+        for (int k = 0; k < kScanAhead; ++k)
+            if (c0 + k < a.nch) S[k] = __ldcs(w + (c0 + k) * cstride);
 #pragma unroll
-        for (int k = 0; k < kScanPerThread; ++k) {
-            const long long e = e0 + (long long)k * kScanThreads;
-            S[k] = e < a.PN ? __ldcs(w + c * cstride + e) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kScanPerThread; ++k) {
-            const long long e = e0 + (long long)k * kScanThreads;
-            if (e < a.PN) w[c * cstride + e] = Hs[k];
-            Hs[k] = fmaf(l, Hs[k], S[k]);
+        for (int k = 0; k < kScanAhead; ++k) {
+            if (c0 + k < a.nch) {
+                w[(c0 + k) * cstride] = H;
+                H = fma4(lam[c0 + k], H, S[k]);
+            }
         }
     }
-    if (ok) {
-#pragma unroll
-        for (int k = 0; k < kScanPerThread; ++k) {
-            const long long e = e0 + (long long)k * kScanThreads;
-            if (e < a.PN) cache[e] = Hs[k];
-        }
-    }
+    if (ok) *cache = H;
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -1426,7 +1419,7 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     sa.nch = nch;
     sa.L = L;
     sa.PN = P * N;
-    const dim3 grid((unsigned)((P * N + kScanThreads * kScanPerThread - 1) / (kScanThreads * kScanPerThread)),
+    const dim3 grid((unsigned)((P * N / kScanPerThread + kScanThreads - 1) / kScanThreads),
                     (unsigned)H, (unsigned)Bn);
     ssm_chunk_scan_kernel<<<grid, kScanThreads, nch * sizeof(float), static_cast<cudaStream_t>(stream)>>>(sa);
     const cudaError_t e = cudaGetLastError();
