@@ -210,15 +210,17 @@ def hbm_peak():
 
 
 HOST_MARKER = "// ----------------------------------------------------------------------------- host side"
+PREFILL_MARKER = "// ----------------------------------------------------------------------------- prefill kernels"
 
 
 def kernel_source_hash(path: str = KERNEL_SRC) -> str:
-    """sha256 of the device code of a kernel source: the text before its
-    host-side section, with #include lines left out, so that host-only edits
-    keep a recorded capture valid while any kernel edit voids it."""
+    """sha256 of the tile kernel's device code: the text before the source's
+    prefill kernels (or its host-side section), with #include lines left out,
+    so that host-only and prefill-only edits keep a recorded capture valid
+    while any edit of the tile kernel voids it."""
     with open(path) as f:
         text = f.read()
-    dev = text.split(HOST_MARKER)[0]
+    dev = text.split(PREFILL_MARKER)[0].split(HOST_MARKER)[0]
     dev = "\n".join(line for line in dev.splitlines() if not line.startswith("#include"))
     return hashlib.sha256(dev.encode()).hexdigest()
 

@@ -966,6 +966,135 @@ __global__ void ssm_wait_timeout_kernel(uint32_t *status) {
 }
 
 
+// ----------------------------------------------------------------------------- prefill kernels
+
+// Chunked prefill, first pass on the tensor cores: the state a chunk of L
+// tokens leaves when it starts from h = 0 -- the recurrence unrolled over
+// the chunk,
+//     S[p][n] = sum_s w_s u_s[p] B_s[n],   w_s = prod_{r > s} Abar_r,   u_s = dt_s x_s,
+// -- as one contraction over the chunk's tokens, (w o U) (rows x L) times
+// B (L x N), on mma.sync m16n8k8 tf32 with fp32 accumulation. w o U is split
+// into tf32 high and low parts so that the products keep fp32 accuracy; bf16
+// B is exact in tf32, fp32 B is split as well. One 64-row tile of one head
+// of one chunk per CTA (16 rows per warp; a thread's accumulators are the
+// state-register layout of the tile kernel).
+constexpr int kCSRows = 64;
+constexpr int kCSMaxL = 128;
+
+struct CSArgs {
+    const void *x, *B, *dt;  // chunk v = tokens v*L .. v*L + L - 1 of the [batch][T] layouts
+    const float *A;
+    float *ws;               // [chunks][H][P][N]
+    int H, P, G, L, ptiles;
+};
+
+template <typename Tin, int N>
+struct CSLay {
+    static constexpr int kXPad = kCSRows + 8;  // x staged token-major, rows padded: conflict-free fragments
+    static constexpr int kBPad = N + 8;
+    static constexpr int kX = 0;
+    static constexpr int kB = kX + kCSMaxL * kXPad * (int)sizeof(Tin);
+    static constexpr int kW = kB + kCSMaxL * kBPad * (int)sizeof(Tin);
+    static constexpr int kW2 = kW + kCSMaxL * 4;  // second buffer of the suffix-product scan
+    static constexpr int kDt = kW2 + kCSMaxL * 4;
+    static constexpr int kBytes = kDt + kCSMaxL * 4;
+    static_assert(kB % 16 == 0 && (kXPad * sizeof(Tin)) % 16 == 0 && (kBPad * sizeof(Tin)) % 16 == 0, "alignment");
+};
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ float sval(const float *p) { return *p; }
+__device__ __forceinline__ float sval(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+template <typename Tin, int N>
+__global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
+    using LY = CSLay<Tin, N>;
+    constexpr int NB = N / 8;
+    constexpr int VW = 16 / (int)sizeof(Tin);  // elements per 16-byte vector
+    Tin *sx = sm<Tin>(LY::kX);
+    Tin *sb = sm<Tin>(LY::kB);
+    float *sw = sm<float>(LY::kW), *sw2 = sm<float>(LY::kW2), *sdt = sm<float>(LY::kDt);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
+    const long long t = blockIdx.x;
+    const int ptile = (int)(t % a.ptiles);
+    const long long vh = t / a.ptiles;
+    const int h = (int)(vh % a.H);
+    const long long v = vh / a.H;
+    const int gi = h / (a.H / a.G);
+    const int row0 = ptile * kCSRows;
+    const int L = a.L;
+    const float Ah = __ldg(a.A + h);
+    const Tin *x = static_cast<const Tin *>(a.x);
+    const Tin *Bp = static_cast<const Tin *>(a.B);
+    const Tin *dtp = static_cast<const Tin *>(a.dt);
+
+    // stage the chunk's x rows (this tile's 64 rows) and B rows, 16 bytes at a time
+    for (int i = tid; i < L * (kCSRows / VW); i += 128) {
+        const int s = i / (kCSRows / VW), q = i % (kCSRows / VW);
+        cp_async16(sx + s * LY::kXPad + q * VW, x + ((v * L + s) * a.H + h) * (long long)a.P + row0 + q * VW);
+    }
+    for (int i = tid; i < L * (N / VW); i += 128) {
+        const int s = i / (N / VW), q = i % (N / VW);
+        cp_async16(sb + s * LY::kBPad + q * VW, Bp + ((v * L + s) * a.G + gi) * (long long)N + q * VW);
+    }
+    // dt and the suffix products w_s = prod_{r > s} Abar_r (a fixed product tree)
+    if (tid < L) {
+        const float d = ld1(dtp + (v * L + tid) * a.H + h);
+        sdt[tid] = d;
+        sw[tid] = tid + 1 < L ? ssm_decay(ld1(dtp + (v * L + tid + 1) * a.H + h), Ah) : 1.f;
+    }
+    __syncthreads();
+    float *cur = sw, *nxt = sw2;
+    for (int d = 1; d < L; d <<= 1) {
+        if (tid < L) nxt[tid] = tid + d < L ? __fmul_rn(cur[tid], cur[tid + d]) : cur[tid];
+        __syncthreads();
+        float *tmp = cur;
+        cur = nxt;
+        nxt = tmp;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+    const int r0 = warp * 16 + g, r1 = r0 + 8;
+    for (int kb = 0; kb < L / 8; ++kb) {
+        const int s0 = kb * 8 + tq, s1 = s0 + 4;
+        const float w0 = cur[s0], w1 = cur[s1], d0 = sdt[s0], d1 = sdt[s1];
+        const Split a0 = split(__fmul_rn(w0, ssm_input_scale(d0, sval(sx + s0 * LY::kXPad + r0))));
+        const Split a1 = split(__fmul_rn(w0, ssm_input_scale(d0, sval(sx + s0 * LY::kXPad + r1))));
+        const Split a2 = split(__fmul_rn(w1, ssm_input_scale(d1, sval(sx + s1 * LY::kXPad + r0))));
+        const Split a3 = split(__fmul_rn(w1, ssm_input_scale(d1, sval(sx + s1 * LY::kXPad + r1))));
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const float b0 = sval(sb + s0 * LY::kBPad + nb * 8 + g), b1 = sval(sb + s1 * LY::kBPad + nb * 8 + g);
+            if constexpr (sizeof(Tin) == 2) {  // bf16 values are exact in tf32
+                const uint32_t e0 = __float_as_uint(b0), e1 = __float_as_uint(b1);
+                mma_tf32(acc[nb], a0.hi, a1.hi, a2.hi, a3.hi, e0, e1);
+                mma_tf32(acc[nb], a0.lo, a1.lo, a2.lo, a3.lo, e0, e1);
+            } else {
+                const Split c0 = split(b0), c1 = split(b1);
+                mma_tf32(acc[nb], a0.hi, a1.hi, a2.hi, a3.hi, c0.hi, c1.hi);
+                mma_tf32(acc[nb], a0.lo, a1.lo, a2.lo, a3.lo, c0.hi, c1.hi);
+                mma_tf32(acc[nb], a0.hi, a1.hi, a2.hi, a3.hi, c0.lo, c1.lo);
+            }
+        }
+    }
+    float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0) * N;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int c = nb * 8 + 2 * tq;
+        *reinterpret_cast<float2 *>(out + (long long)r0 * N + c) = make_float2(acc[nb][0], acc[nb][1]);
+        *reinterpret_cast<float2 *>(out + (long long)r1 * N + c) = make_float2(acc[nb][2], acc[nb][3]);
+    }
+}
+
 // Chunked prefill, the pass between the chunk passes: carry the state across a
 // prompt's chunks. Chunk c of sequence b, started from h = 0, left S_c in
 // ws[b * nch + c]; with lambda_c the product of its tokens' Abar,
