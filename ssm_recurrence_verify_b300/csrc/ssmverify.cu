@@ -1455,7 +1455,7 @@ int64_t prefill_ws_bytes(const ssm_desc_t *d, int L) {
     return prefill_ws_states(d, L) + ((int64_t)d->batch * (d->ntok / L) * 4 + 15) / 16 * 16;
 }
 
-// Chunk length of a chunked prefill: the largest of 256, 128, 64, 32, 16
+// Chunk length of a chunked prefill: the largest of 128, 64, 32, 16
 // that divides the prompt into at least two chunks, fits the workspace and
 // gives one wave of tiles (four per SM); the smallest fitting one if none
 // reaches a wave. 0: the one-pass form (it fills the device by itself, or no
@@ -1468,13 +1468,46 @@ int prefill_chunk_len(const ssm_desc_t *d, int64_t ws_bytes) {
     const int64_t wave = (int64_t)device_sms() * 4;
     if (wave <= 0 || base >= wave) return 0;
     int best = 0;
-    for (int L = 256; L >= 16; L >>= 1) {
+    for (int L = kCSMaxL; L >= 16; L >>= 1) {
         if (T % L != 0 || T / L < 2 || T / L > kMaxChunks) continue;
         if (ws_bytes >= 0 && prefill_ws_bytes(d, L) > ws_bytes) continue;
         best = L;
         if (base * (T / L) >= wave) break;
     }
     return best;
+}
+
+template <typename Tin, int N>
+cudaError_t launch_cs_t(const CSArgs &a, long long ntiles, cudaStream_t s) {
+    constexpr int SMEM = CSLay<Tin, N>::kBytes;
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || ready[dev].load(std::memory_order_relaxed) == 0) {
+        e = cudaFuncSetAttribute(ssm_chunk_state_kernel<Tin, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_relaxed);
+    }
+    ssm_chunk_state_kernel<Tin, N><<<(unsigned)ntiles, 128, SMEM, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_state(int in_dtype, int N, const CSArgs &a, long long ntiles, cudaStream_t s) {
+    if (in_dtype == SSM_BF16) {
+        switch (N) {
+            case 16: return launch_cs_t<__nv_bfloat16, 16>(a, ntiles, s);
+            case 32: return launch_cs_t<__nv_bfloat16, 32>(a, ntiles, s);
+            case 64: return launch_cs_t<__nv_bfloat16, 64>(a, ntiles, s);
+            default: return launch_cs_t<__nv_bfloat16, 128>(a, ntiles, s);
+        }
+    }
+    switch (N) {
+        case 16: return launch_cs_t<float, 16>(a, ntiles, s);
+        case 32: return launch_cs_t<float, 32>(a, ntiles, s);
+        case 64: return launch_cs_t<float, 64>(a, ntiles, s);
+        default: return launch_cs_t<float, 128>(a, ntiles, s);
+    }
 }
 
 int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
@@ -1528,8 +1561,30 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     c1.xr = x; c1.Br = B; c1.dtr = dt;
     c1.A = A;
     c1.dev_status = dev_status;
-    rc = run(&dv, c1, stream);
-    if (rc != SSM_OK) return rc;
+    const bool cs_ok = N <= 128 && P % kCSRows == 0 && aligned(x, 16) && aligned(B, 16) && (P * eb) % 16 == 0 &&
+                       aligned(dt, eb);
+    if (cs_ok) {
+        CSArgs ca;
+        ca.x = x;
+        ca.B = B;
+        ca.dt = dt;
+        ca.A = A;
+        ca.ws = static_cast<float *>(ws);
+        ca.H = (int)H;
+        ca.P = (int)P;
+        ca.G = (int)G;
+        ca.L = L;
+        ca.ptiles = (int)(P / kCSRows);
+        const long long nt = (long long)dv.batch * H * (P / kCSRows);
+        const cudaError_t e1 = launch_chunk_state(d->in_dtype, (int)N, ca, nt, static_cast<cudaStream_t>(stream));
+        if (e1 != cudaSuccess) {
+            g_last_cuda_error = (int)e1;
+            return SSM_ERR_CUDA;
+        }
+    } else {
+        rc = run(&dv, c1, stream);
+        if (rc != SSM_OK) return rc;
+    }
 
     ScanArgs sa;
     sa.pool = pool->states;
