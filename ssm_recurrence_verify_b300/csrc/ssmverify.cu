@@ -71,6 +71,7 @@ enum Flavour : int {
 // (a pool), and every tile starts from h = 0 without reading a state.
 constexpr int kPoolBit = 8;
 constexpr int kZeroBit = 16;
+constexpr int kMmaBit = 32;  // verify phase: the state crosses full chunks on the tensor cores (N <= 128)
 
 template <int F>
 struct Flav {
@@ -80,6 +81,7 @@ struct Flav {
     static constexpr bool kWriteInVerify = kBase == kVerifyCommit;
     static constexpr bool kPool = (F & kPoolBit) != 0;
     static constexpr bool kZero = (F & kZeroBit) != 0;
+    static constexpr bool kMmaAdvance = (F & kMmaBit) != 0;
 };
 
 // Per-N geometry. A band is 16 rows (one mma M block); WPB warps share a
@@ -607,6 +609,66 @@ __device__ __forceinline__ Split split(float x) {
     return s;
 }
 
+// Advance the register state over the staged chunk (tc tokens) on the tensor
+// cores -- the recurrence regrouped over the chunk:
+//     h <- lambda h + sum_s w_s u_s B_s^T,   lambda = prod_s Abar_s,   w_s = prod_{r > s} Abar_r
+// as one rank-8 update, mma.sync m16n8k8 tf32 with the state itself as the
+// accumulator. The thread's slot pair (2 nb, 2 nb + 1) of rows g and g + 8 is
+// the D fragment of n-block nb under the column permutation of the staged B
+// (logical column j of n-block nb is physical column
+// 4 (j / 2) + 16 (nb / 2) + 2 (nb % 2) + j % 2, staged at row j / 2, slot
+// 2 nb + j % 2), so no state moves. w o u is split into tf32 high and low
+// parts; bf16 B is exact in tf32, fp32 B is split as well. Layouts with one
+// warp per band (N <= 128) only.
+template <typename Tin, int N>
+__device__ __forceinline__ void advance_mma(float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L, const StagedOffsets &so,
+                                            int tc) {
+    using G = Geo<N>;
+    static_assert(G::kWPB == 1, "one warp per band");
+    constexpr int ROWS = G::kRows;
+    const float *abar = sm<const float>(so.Abar);
+    const int t0 = L.tq, t1 = L.tq + 4;  // this thread's two tokens of the A fragment
+    float w0 = 0.f, w1 = 0.f, lam = 1.f;  // w = 0 past tc (u is zero there too)
+#pragma unroll
+    for (int t = kTC - 1; t >= 0; --t) {
+        if (t < tc) {
+            if (t == t0) w0 = lam;
+            if (t == t1) w1 = lam;
+            lam = __fmul_rn(lam, abar[t]);
+        }
+    }
+    const float2 l2 = make_float2(lam, lam);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int m = 0; m < G::kNC / 2; ++m) hs[rr][m] = __fmul2_rn(hs[rr][m], l2);
+    const float *U = sm<const float>(so.U);
+    const int r0 = L.band * 16 + L.g, r1 = r0 + 8;
+    const Split a0 = split(__fmul_rn(w0, U[t0 * ROWS + r0]));
+    const Split a1 = split(__fmul_rn(w0, U[t0 * ROWS + r1]));
+    const Split a2 = split(__fmul_rn(w1, U[t1 * ROWS + r0]));
+    const Split a3 = split(__fmul_rn(w1, U[t1 * ROWS + r1]));
+    const float *Bs = sm<const float>(so.B);
+    const int col = (L.g >> 1) * G::kPad + (L.g & 1);
+    const float *b0p = Bs + t0 * 4 * G::kPad + col, *b1p = Bs + t1 * 4 * G::kPad + col;
+#pragma unroll
+    for (int nb = 0; nb < G::kNC / 2; ++nb) {
+        const float b0 = b0p[2 * nb], b1 = b1p[2 * nb];
+        float d[4] = {hs[0][nb].x, hs[0][nb].y, hs[1][nb].x, hs[1][nb].y};
+        if constexpr (sizeof(Tin) == 2) {
+            mma_tf32(d, a0.hi, a1.hi, a2.hi, a3.hi, __float_as_uint(b0), __float_as_uint(b1));
+            mma_tf32(d, a0.lo, a1.lo, a2.lo, a3.lo, __float_as_uint(b0), __float_as_uint(b1));
+        } else {
+            const Split c0 = split(b0), c1 = split(b1);
+            mma_tf32(d, a0.hi, a1.hi, a2.hi, a3.hi, c0.hi, c1.hi);
+            mma_tf32(d, a0.lo, a1.lo, a2.lo, a3.lo, c0.hi, c1.hi);
+            mma_tf32(d, a0.hi, a1.hi, a2.hi, a3.hi, c0.lo, c1.lo);
+        }
+        hs[0][nb] = make_float2(d[0], d[1]);
+        hs[1][nb] = make_float2(d[2], d[3]);
+    }
+}
+
 // y for the staged verify chunk (tc tokens, chunk start state hs):
 //   y_t = w_t (C_t . h) + sum_{s<=t} L[t,s] (C_t . B_s) u_s + D x_t
 // h . C^T and C . B^T on the tensor cores; y stored to ychunk + t * ystride + row.
@@ -939,6 +1001,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
                 int steps = 0;
                 if (t0 + tc < K) steps = tc;
                 else if (FL::kWriteInVerify && jw >= t0) steps = jw - t0 + 1;
+                if constexpr (FL::kMmaAdvance && G::kWPB == 1) {
+                    if (t0 + tc < K) {  // the next chunk starts from h after this one: no state is written here
+                        advance_mma<Tin, N>(hs, L, sV, tc);
+                        steps = 0;
+                    }
+                }
 #pragma unroll 1
                 for (int s = 0; s < steps; ++s) {
                     recur_token<N>(hs, L, sV, s);
@@ -1304,6 +1372,7 @@ struct Call {
     int nslots = 0;
     bool zero_state = false;        // internal: every tile starts from h = 0, nothing is read
     bool accept_all = false;        // internal: the replay block is replayed in full (no accept_len)
+    bool mma_advance = false;       // internal (verify, N <= 128): full chunks crossed on the tensor cores
 };
 
 // Validate everything on the host, then launch (with dry: validate only).
@@ -1410,7 +1479,8 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    const int FX = F | (c.pool ? kPoolBit : 0) | (c.zero_state ? kZeroBit : 0);
+    const int FX = F | (c.pool ? kPoolBit : 0) | (c.zero_state ? kZeroBit : 0) |
+                   (c.mma_advance && d->dstate <= 128 ? kMmaBit : 0);
     switch (FX) {
         case kVerify: e = launch_flavour<kVerify>(d->in_dtype, N, a, s); break;
         case kCommit: e = launch_flavour<kCommit>(d->in_dtype, N, a, s); break;
@@ -1421,6 +1491,8 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
         case kCommitVerify | kPoolBit: e = launch_flavour<kCommitVerify | kPoolBit>(d->in_dtype, N, a, s); break;
         case kVerifyCommit | kPoolBit: e = launch_flavour<kVerifyCommit | kPoolBit>(d->in_dtype, N, a, s); break;
         case kCommit | kZeroBit: e = launch_flavour<kCommit | kZeroBit>(d->in_dtype, N, a, s); break;
+        case kVerify | kMmaBit: e = launch_flavour<kVerify | kMmaBit>(d->in_dtype, N, a, s); break;
+        case kVerify | kPoolBit | kMmaBit: e = launch_flavour<kVerify | kPoolBit | kMmaBit>(d->in_dtype, N, a, s); break;
         default: return SSM_ERR_UNSUPPORTED;  // no kernel for this combination
     }
     if (e != cudaSuccess) {
@@ -1615,6 +1687,7 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     Call c3{};
     c3.flavour = kVerify;
     c3.state_in = static_cast<const float *>(ws);
+    c3.mma_advance = true;
     if (vslot != nullptr) {  // chunks of sequences without a valid slot write no y
         c3.pool = true;
         c3.slot = vslot;

@@ -154,6 +154,15 @@ def test_prefill_matches_oracle(cuda_device, T, dtype):
     _prefill_case(cuda_device, 2, 4, 64, 128, 2, T, dtype, seed=400 + T)
 
 
+@pytest.mark.parametrize("N,P,dtype", [(16, 64, synth.F32), (64, 128, synth.BF16), (256, 64, synth.BF16),
+                                         (128, 96, synth.BF16)])
+def test_prefill_other_geometries(cuda_device, N, P, dtype):
+    """State sizes whose chunk passes take other layouts: N = 16 and 64 (one
+    warp per band), N = 256 (two warps per band: the chunk passes use the
+    recurrence), and P = 96 (not a multiple of the 64-row tile)."""
+    _prefill_case(cuda_device, 2, 4, P, N, 2, 256, dtype, seed=480 + N + P)
+
+
 def test_prefill_chunked_and_one_pass_agree(cuda_device):
     """The chunked regrouping and the plain recurrence agree to rounding, and
     the small shape really does take the chunked form."""
