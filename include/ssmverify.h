@@ -38,7 +38,8 @@
  * caller (for the whole time the launched work runs). The library allocates
  * nothing, frees nothing and never synchronises; the only state it keeps
  * between calls is a cache of immutable device properties (SM count and
- * resident blocks per SM, per kernel and device), so calls are thread-safe.
+ * resident blocks per SM, per kernel and device), so calls are thread-safe
+ * (ssm_prefill_scratch alone also uses a fixed device array; see there).
  * Every entry point only validates its arguments and enqueues one kernel (ssm_prefill: up to three) on
  * `stream` (a cudaStream_t passed as void*, NULL = the legacy default
  * stream) on the current device. Calls are asynchronous.
@@ -231,6 +232,21 @@ int64_t ssm_prefill_workspace_bytes(const ssm_desc_t *desc);
 int ssm_prefill(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
                 const void *dt, const float *A, const float *D, float *y, void *workspace, int64_t workspace_bytes,
                 uint32_t *dev_status, void *stream);
+
+/*
+ * ssm_prefill_scratch -- ssm_prefill without a caller workspace: the chunked
+ * form runs in a fixed device array of SSM_PREFILL_SCRATCH_BYTES inside the
+ * library (allocated with the library's device code, once per device).
+ * Shapes whose chunked workspace (ssm_prefill_workspace_bytes) exceeds it are
+ * rejected with SSM_ERR_SHAPE before anything is launched; nothing in the
+ * array needs to start at zero. Calls that may overlap in time (other
+ * streams, other host threads, other processes sharing the context) race on
+ * the array: issue them one after another. The pages have no counterpart;
+ * this exists for callers that cannot allocate device memory.
+ */
+#define SSM_PREFILL_SCRATCH_BYTES (64ll << 20)
+int ssm_prefill_scratch(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                        const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream);
 
 /*
  * ssm_selftest_wait_timeout -- failure-detection self-test of the bounded

@@ -1243,6 +1243,11 @@ __global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const Scan
     if (ok) *cache = H;
 }
 
+// Fixed device scratch of ssm_prefill_scratch: the chunked prefill's
+// workspace for callers that do not allocate one. Calls using it must not
+// overlap in time: they would share it.
+static __device__ __align__(256) unsigned char g_prefill_scratch[SSM_PREFILL_SCRATCH_BYTES];
+
 // ----------------------------------------------------------------------------- host side
 
 thread_local int g_last_cuda_error = 0;
@@ -1699,6 +1704,21 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     return run(&dv, c3, stream);
 }
 
+// Device address of the prefill scratch on the current device (cached per device).
+void *prefill_scratch(cudaError_t &err) {
+    static std::atomic<void *> cache[kMaxDevices];
+    int dev = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return nullptr;
+    void *p = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : nullptr;
+    if (p == nullptr) {
+        err = cudaGetSymbolAddress(&p, g_prefill_scratch);
+        if (err != cudaSuccess) return nullptr;
+        if (dev >= 0 && dev < kMaxDevices) cache[dev].store(p, std::memory_order_relaxed);
+    }
+    return p;
+}
+
 Call pool_call(int flavour, const ssm_pool_t *pool) {
     Call c{};
     c.flavour = flavour;
@@ -1866,6 +1886,26 @@ int ssm_prefill(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, c
                 const void *dt, const float *A, const float *D, float *y, void *workspace, int64_t workspace_bytes,
                 uint32_t *dev_status, void *stream) {
     return prefill(desc, pool, x, B, C, dt, A, D, y, workspace, workspace_bytes, dev_status, stream);
+}
+
+int ssm_prefill_scratch(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,
+                        const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream) {
+    const int rc = check_desc(desc);
+    if (rc != SSM_OK) return rc;
+    if (pool == nullptr) return SSM_ERR_NULL;
+    if (desc->batch == 0) return SSM_OK;
+    const int64_t need = ssm_prefill_workspace_bytes(desc);
+    if (need > SSM_PREFILL_SCRATCH_BYTES) return SSM_ERR_SHAPE;  // more than the fixed scratch holds
+    void *ws = nullptr;
+    if (need > 0) {
+        cudaError_t e = cudaSuccess;
+        ws = prefill_scratch(e);
+        if (ws == nullptr) {
+            g_last_cuda_error = (int)e;
+            return SSM_ERR_CUDA;
+        }
+    }
+    return prefill(desc, pool, x, B, C, dt, A, D, y, ws, need, dev_status, stream);
 }
 
 int ssm_selftest_wait_timeout(uint32_t *dev_status, void *stream) {

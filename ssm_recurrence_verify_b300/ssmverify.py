@@ -35,10 +35,11 @@ SSM_STATUS_BAD_TOKEN = 4
 SSM_STATUS_BAD_SLOT = 8
 SSM_ACCEPT_MAX_NTOK = 32
 SSM_ACCEPT_MAX_VOCAB = 1 << 28
+SSM_PREFILL_SCRATCH_BYTES = 64 << 20
 
 EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
            "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool", "ssm_step_pool",
-           "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_selftest_wait_timeout", "ssm_accept_greedy",
+           "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_scratch", "ssm_selftest_wait_timeout", "ssm_accept_greedy",
            "ssm_accept_sample", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
 
 
@@ -94,11 +95,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_commit_verify_pool.argtypes = [dp, pp, ctypes.c_int32] + [vp] * 13
     lib.ssm_step_pool.argtypes = [dp, pp] + [vp] * 9
     lib.ssm_prefill.argtypes = [dp, pp] + [vp] * 8 + [ctypes.c_int64, vp, vp]
+    lib.ssm_prefill_scratch.argtypes = [dp, pp] + [vp] * 9
     lib.ssm_prefill_workspace_bytes.argtypes = [dp]
     lib.ssm_prefill_workspace_bytes.restype = ctypes.c_int64
     for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
               "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool",
-              "ssm_step_pool", "ssm_prefill", "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample",
+              "ssm_step_pool", "ssm_prefill", "ssm_prefill_scratch", "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample",
               "ssm_last_cuda_error", "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
@@ -428,4 +430,16 @@ def prefill(states, slot, x, B, C, dt, A, D, y=None, workspace=None, dev_status=
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.ssm_prefill(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A),
                            _ptr(D), _ptr(y), _ptr(workspace), wbytes, _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def prefill_scratch(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
+    """prefill with the library's fixed device scratch as the workspace
+    (nothing is allocated for it). Calls must not overlap in time; shapes
+    whose workspace exceeds SSM_PREFILL_SCRATCH_BYTES are rejected."""
+    y = _new_y(states, x) if y is None else y
+    desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
+    pool = _pool(states, slot, x.shape[0])
+    _check(load_library().ssm_prefill_scratch(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
+                                              _ptr(dt), _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
