@@ -16,22 +16,30 @@
 // accept_len lands in device memory, ready for ssm_commit /
 // ssm_commit_verify without a trip through the host.
 //
-// Kernel design (B300; bound by the HBM stream of the logits):
+// Kernel design (B300; bound by the HBM stream of the logits it must read):
 //  * One thread-block cluster of kCl CTAs per sequence; CTA r owns a slice
-//    of V / kCl vocabulary entries of every row (the K + 1 verifier rows, and
-//    for sampling the K draft rows) and streams it once with 16-byte loads,
-//    kAU of them in flight per thread.
+//    of V / kCl vocabulary entries of every row and streams it with 16-byte
+//    loads, kAU of them in flight per thread.
+//  * The rule only ever looks at rows up to the first rejection, so the
+//    rows are read in steps of kGroup draft tokens (their verifier rows and,
+//    for sampling, their draft rows) and the walk stops at the step holding
+//    the first rejection: rows past it are never read. (One token per step
+//    exposes a load latency and a cluster barrier per token; three per step
+//    measured fastest.)
 //  * Per row, each thread keeps a running (max, sum of exp(l - max)) -- the
 //    online softmax normaliser -- or a running (max, first index of the
 //    max); warps, then the CTA, then the cluster combine these partials. The
 //    cluster step reads every CTA's partials through distributed shared
 //    memory in rank order, so every CTA of the cluster holds bit-identical
 //    row statistics and takes the same decisions without further exchange.
+//    The partials of consecutive steps alternate between two buffers, so one
+//    cluster barrier per step suffices.
 //  * Sampling then draws the next token: every CTA sums the weights of its
-//    slice (each thread a contiguous run, a block prefix over threads, a
-//    cluster prefix over CTAs); the CTA and thread whose range holds the
-//    threshold rescan that run. The search uses the same rounded partial sums
-//    at every level, so it always ends on an index of positive weight.
+//    slice of row j (each thread a contiguous run, a block prefix over
+//    threads, a cluster prefix over CTAs); the CTA and thread whose range
+//    holds the threshold rescan that run. The search uses the same rounded
+//    partial sums at every level, so it always ends on an index of positive
+//    weight.
 //  * exp(l - m) is taken as 2^(l log2 e - m log2 e) with the hardware's base-2
 //    exponential (PTX ex2.approx, relative error about 2^-22, subnormal
 //    results flushed to zero): the change of base used by fused softmax
@@ -57,7 +65,7 @@ constexpr int kAWarps = kAT / 32;
 constexpr int kAU = 8;                               // 16-byte loads in flight per thread and batch
 constexpr int kAS = 16;                              // elements per thread and batch on the scalar path
 constexpr int kCl = 8;                               // CTAs per sequence (one cluster)
-constexpr int kMaxRows = 2 * SSM_ACCEPT_MAX_NTOK + 1;
+constexpr int kGroup = 3;                            // draft tokens whose rows are read and decided per step
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kEmpty = -1.0e30f;                   // running max of a partial that has seen nothing
 constexpr int kNoIndex = INT_MAX;
@@ -404,12 +412,12 @@ __device__ float run_weights(const T *prow, const T *qrow, int e_lo, int e_hi, c
 
 template <typename T, bool SAMPLE, bool VEC>
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept_kernel(const AArgs a) {
-    __shared__ float2 wpart[kMaxRows][kAWarps];   // per row: one partial per warp
-    __shared__ float2 cpart[kMaxRows];            // per row: this CTA's partial (read by the whole cluster)
-    __shared__ float2 fin[kMaxRows];              // per row: the sequence's statistics
+    __shared__ float2 wpart[2 * kGroup][kAWarps];  // this step's rows: one partial per warp
+    __shared__ float2 cpart[2][2 * kGroup];        // [step parity][row]: this CTA's partials, read by the cluster
+    __shared__ float2 fin[2 * kGroup];             // this step's row statistics for the sequence
     __shared__ float wsum[kAWarps];
-    __shared__ float cW;                          // this CTA's total weight (read by the whole cluster)
-    __shared__ int s_j, s_bad, s_owner, s_first, s_last;
+    __shared__ float cW;                  // this CTA's total weight (read by the whole cluster)
+    __shared__ int s_rej, s_bad, s_owner, s_first, s_last;
     __shared__ float s_P, s_thr;
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -417,14 +425,14 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
     const int b = (int)(blockIdx.x / kCl);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = a.K, V = a.V;
-    const int R = SAMPLE ? 2 * K + 1 : K + 1;
     const T *tl = static_cast<const T *>(a.tl) + (int64_t)b * (K + 1) * V;
     const T *ql = SAMPLE ? static_cast<const T *>(a.ql) + (int64_t)b * K * V : nullptr;
     const int lo = min(rank * a.slice, V), hi = min(lo + a.slice, V);
     constexpr int W = VEC ? Logit<T>::W : 1;
 
-    // ---- phase 0: the logits at the draft tokens, which the acceptance
-    // rule reads; loaded now (warp 0, one token per lane), used after phase 1.
+    // ---- the logits at the draft tokens and the uniforms, which the
+    // acceptance rule reads: loaded first (warp 0, lane t for token t) so that
+    // their latency hides behind the first row pass.
     int pre_x = -1;
     float pre_lp = 0.f, pre_lq = 0.f, pre_u = 0.f;
     if (warp == 0 && lane < K) {
@@ -436,111 +444,121 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
         }
     }
 
-    // ---- phase 1: per-row partials of this CTA's slice. Rows run from the
-    // bonus position down to 0 so that the rows a rejection most often picks
-    // are the most recently read when the next-token draw re-reads them.
-    {
-        using Bt = Batch<T, VEC>;
-        using Acc = typename std::conditional<SAMPLE, SoftAcc, ArgAcc>::type;
-        const int ulo = lo / W, uhi = hi / W;  // slice in load units (vectors, or elements)
-        for (int step = 0; step < R; ++step) {
-            int row;  // t for verifier row t, K + 1 + t for draft row t
-            if (step == 0) {
-                row = K;
-            } else {
-                const int t = K - 1 - (step - 1) / (SAMPLE ? 2 : 1);
-                row = (SAMPLE && ((step - 1) & 1) == 0) ? K + 1 + t : t;
+    // ---- steps t = 0, 1, ...: the statistics of verifier row t (and draft
+    // row t), then the decision on draft token t. The first rejection ends
+    // the walk: rows past it are never read. Every CTA combines the cluster's
+    // partials in rank order, so all take the same decisions.
+    using Bt = Batch<T, VEC>;
+    using Acc = typename std::conditional<SAMPLE, SoftAcc, ArgAcc>::type;
+    const int ulo = lo / W, uhi = hi / W;  // slice in load units (vectors, or elements)
+    // Step: tokens t0 .. t0 + ng - 1; row 2i is verifier row t0 + i, row
+    // 2i + 1 draft row t0 + i (sampling, t0 + i < K).
+    int j = K, badj = 0, jrow = 0;
+    for (int t0 = 0; t0 <= K; t0 += kGroup) {
+        const int ng = min(kGroup, K + 1 - t0);
+        for (int i = 0; i < ng; ++i) {
+            const int nr = (SAMPLE && t0 + i < K) ? 2 : 1;
+            for (int r = 0; r < nr; ++r) {
+                const T *src = (r == 0 ? tl : ql) + (int64_t)(t0 + i) * V;
+                Acc acc;
+                for (int u0 = ulo + tid; u0 < uhi; u0 += Bt::S * kAT) {
+                    Bt bt;
+                    bt.load(src, u0, uhi);
+                    acc.push(bt);
+                }
+                const float2 out = acc.warp_total();
+                if (lane == 0) wpart[2 * i + r][warp] = out;
             }
-            const T *src = row <= K ? tl + (int64_t)row * V : ql + (int64_t)(row - K - 1) * V;
-            Acc acc;
-            for (int u0 = ulo + tid; u0 < uhi; u0 += Bt::S * kAT) {
-                Bt bt;
-                bt.load(src, u0, uhi);
-                acc.push(bt);
+        }
+        __syncthreads();
+        const int par = (t0 / kGroup) & 1;
+        auto rowvalid = [&](int q) { return q / 2 < ng && (q % 2 == 0 || (SAMPLE && t0 + q / 2 < K)); };
+        if (tid < 2 * kGroup && rowvalid(tid)) {
+            float2 c = wpart[tid][0];
+            for (int w = 1; w < kAWarps; ++w) {
+                const float2 o = wpart[tid][w];
+                if (SAMPLE) {
+                    soft_combine(c.x, c.y, o.x, o.y);
+                } else {
+                    int i = __float_as_int(c.y);
+                    arg_combine(c.x, i, o.x, __float_as_int(o.y));
+                    c.y = __int_as_float(i);
+                }
             }
-            const float2 out = acc.warp_total();
-            if (lane == 0) wpart[row][warp] = out;
+            cpart[par][tid] = c;
+        }
+        cluster.sync();  // every CTA's partials of this step are published
+        if (tid < 2 * kGroup && rowvalid(tid)) {
+            float2 c = *cluster.map_shared_rank(&cpart[par][tid], 0);
+            for (int r = 1; r < kCl; ++r) {
+                const float2 o = *cluster.map_shared_rank(&cpart[par][tid], r);
+                if (SAMPLE) {
+                    soft_combine(c.x, c.y, o.x, o.y);
+                } else {
+                    int i = __float_as_int(c.y);
+                    arg_combine(c.x, i, o.x, __float_as_int(o.y));
+                    c.y = __int_as_float(i);
+                }
+            }
+            fin[tid] = c;
+        }
+        __syncthreads();
+        if (warp == 0) {  // lane t holds token t's prefetched values
+            bool rej = false, bad = false;
+            const int i = lane - t0;
+            if (i >= 0 && i < ng && lane < K) {
+                bad = pre_x < 0 || pre_x >= V;
+                if (bad) {
+                    rej = true;
+                } else if (!SAMPLE) {
+                    rej = __float_as_int(fin[2 * i].y) != pre_x;
+                } else {
+                    const float2 fp = fin[2 * i], fq = fin[2 * i + 1];
+                    const float ep = exp2_ftz(fmaf(pre_lp, kLog2e, -(fp.x * kLog2e)));
+                    const float eq = exp2_ftz(fmaf(pre_lq, kLog2e, -(fq.x * kLog2e)));
+                    const float p = __fdiv_rn(ep, fp.y), q = __fdiv_rn(eq, fq.y);
+                    const float ratio = q > 0.f ? __fdiv_rn(p, q) : INFINITY;
+                    rej = !(pre_u < ratio);
+                }
+            }
+            const unsigned m = __ballot_sync(~0u, rej);
+            if (lane == 0) {
+                s_rej = m != 0u ? __ffs(m) - 1 : -1;  // the first rejected token of the step, if any
+            }
+            const int first = m != 0u ? __ffs(m) - 1 : 0;
+            const int fb = __shfl_sync(~0u, bad ? 1 : 0, first);
+            if (lane == 0) s_bad = fb;
+        }
+        __syncthreads();
+        if (s_rej >= 0) {  // the same in every CTA of the cluster
+            j = s_rej;
+            badj = s_bad;
+            jrow = 2 * (j - t0);
+            break;
+        }
+        if (t0 + ng > K) {  // every draft token accepted: row K gives the bonus token
+            jrow = 2 * (K - t0);
+            break;
         }
     }
-    __syncthreads();
-    if (tid < R) {
-        float2 c = wpart[tid][0];
-        for (int w = 1; w < kAWarps; ++w) {
-            const float2 o = wpart[tid][w];
-            if (SAMPLE) {
-                soft_combine(c.x, c.y, o.x, o.y);
-            } else {
-                int i = __float_as_int(c.y);
-                arg_combine(c.x, i, o.x, __float_as_int(o.y));
-                c.y = __int_as_float(i);
-            }
-        }
-        cpart[tid] = c;
-    }
-    cluster.sync();
-    // ---- phase 2: the sequence's row statistics, combined in rank order
-    if (tid < R) {
-        float2 c = *cluster.map_shared_rank(&cpart[tid], 0);
-        for (int r = 1; r < kCl; ++r) {
-            const float2 o = *cluster.map_shared_rank(&cpart[tid], r);
-            if (SAMPLE) {
-                soft_combine(c.x, c.y, o.x, o.y);
-            } else {
-                int i = __float_as_int(c.y);
-                arg_combine(c.x, i, o.x, __float_as_int(o.y));
-                c.y = __int_as_float(i);
-            }
-        }
-        fin[tid] = c;
-    }
-    __syncthreads();
-
-    // ---- phase 3: accept while the rule holds (warp 0; the same in every CTA)
-    if (warp == 0) {
-        bool rej = false, bad = false;
-        if (lane < K) {
-            bad = pre_x < 0 || pre_x >= V;
-            if (bad) {
-                rej = true;
-            } else if (!SAMPLE) {
-                rej = __float_as_int(fin[lane].y) != pre_x;
-            } else {
-                const float2 fp = fin[lane], fq = fin[K + 1 + lane];
-                const float ep = exp2_ftz(fmaf(pre_lp, kLog2e, -(fp.x * kLog2e)));
-                const float eq = exp2_ftz(fmaf(pre_lq, kLog2e, -(fq.x * kLog2e)));
-                const float p = __fdiv_rn(ep, fp.y), q = __fdiv_rn(eq, fq.y);
-                const float ratio = q > 0.f ? __fdiv_rn(p, q) : INFINITY;
-                rej = !(pre_u < ratio);
-            }
-        }
-        const unsigned m = __ballot_sync(~0u, rej);
-        const int j = m != 0u ? __ffs(m) - 1 : K;
-        const int badj = m != 0u ? __shfl_sync(~0u, bad ? 1 : 0, j) : 0;
-        if (lane == 0) {
-            s_j = j;
-            s_bad = badj;
-            if (rank == 0) {
-                a.accept_len[b] = j;
-                if (badj && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_TOKEN);
-                if (!SAMPLE) a.next_token[b] = __float_as_int(fin[j].y);
-            }
-        }
+    if (tid == 0 && rank == 0) {
+        a.accept_len[b] = j;
+        if (badj && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_BAD_TOKEN);
+        if (!SAMPLE) a.next_token[b] = __float_as_int(fin[jrow].y);
     }
     if (!SAMPLE) {
         cluster.sync();  // no CTA leaves while another may still read its partials
         return;
     }
-    __syncthreads();
 
     // ---- phase 4 (sampling): the next token, by inverse CDF at u_K
-    const int j = s_j;
     Weigher wf;
-    wf.resid = j < K && !s_bad;
+    wf.resid = j < K && !badj;
     {
-        const float2 fp = fin[j];
+        const float2 fp = fin[jrow];
         wf.nmlp = -(fp.x * kLog2e);
         wf.invp = __frcp_rn(fp.y);
-        const float2 fq = wf.resid ? fin[K + 1 + j] : make_float2(0.f, 1.f);
+        const float2 fq = wf.resid ? fin[jrow + 1] : make_float2(0.f, 1.f);
         wf.nmlq = -(fq.x * kLog2e);
         wf.invq = __frcp_rn(fq.y);
     }
