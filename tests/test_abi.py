@@ -326,3 +326,44 @@ def test_binding_arities_match_header(lib):
         argtypes = getattr(lib, name).argtypes
         if argtypes is not None:
             assert len(argtypes) == _arity(name), name
+
+
+def pool(states, slot=None, nslots=4, reserved=0):
+    return sv.PoolDesc(states, slot, nslots, reserved)
+
+
+@no_gpu_only
+def test_pool_and_prefill_validation(lib):
+    d = desc()  # batch 2
+    P = ptrs(12)
+    st = P[0].value
+    vcp = lambda pl, p: lib.ssm_verify_commit_pool(ctypes.byref(d), ctypes.byref(pl) if pl is not None else None, *p,
+                                                   None)
+    pre = lambda pl, p, ws=None, wsb=0: lib.ssm_prefill(ctypes.byref(d), ctypes.byref(pl) if pl is not None else None,
+                                                        *p, ws, wsb, None, None)
+    # verify_commit_pool: x, B, C, dt, A, D, accept_len, y, dev_status
+    args = P[1:10]
+    assert vcp(None, args) == sv.SSM_ERR_NULL
+    assert vcp(pool(st, reserved=1), args) == sv.SSM_ERR_SHAPE
+    assert vcp(pool(st, nslots=0), args) == sv.SSM_ERR_SHAPE
+    assert vcp(pool(st, nslots=1), args) == sv.SSM_ERR_SHAPE          # no slot map: nslots >= batch
+    assert vcp(pool(st, slot=P[10].value, nslots=1), args) == sv.SSM_ERR_CUDA  # a slot map: one slot is enough
+    assert vcp(pool(st, slot=P[10].value + 2), args) == sv.SSM_ERR_ALIGN
+    assert vcp(pool(st + 8), args) == sv.SSM_ERR_ALIGN                # states need 16 bytes
+    assert vcp(pool(None), args) == sv.SSM_ERR_NULL
+    a2 = list(args)
+    a2[7] = ctypes.c_void_p(st + 64)                                   # y inside the pool
+    assert vcp(pool(st), a2) == sv.SSM_ERR_ALIAS
+    # prefill: x, B, C, dt, A, D, y
+    pargs = P[1:7] + [P[8]]
+    assert pre(None, pargs) == sv.SSM_ERR_NULL
+    assert pre(pool(st), pargs, None, -1) == sv.SSM_ERR_SHAPE          # negative workspace size
+    assert pre(pool(st, reserved=1), pargs) == sv.SSM_ERR_SHAPE
+    p2 = list(pargs)
+    p2[6] = ctypes.c_void_p(st + 64)                                   # y inside the pool
+    assert pre(pool(st), p2) == sv.SSM_ERR_ALIAS
+    assert pre(pool(st), pargs) == sv.SSM_ERR_CUDA                     # valid: the launch fails on this host
+    d0 = desc(batch=0)
+    assert lib.ssm_prefill(ctypes.byref(d0), ctypes.byref(pool(None)), *([None] * 8), 0, None, None) == sv.SSM_OK
+    assert lib.ssm_prefill_workspace_bytes(ctypes.byref(d0)) == 0
+    assert lib.ssm_prefill_scratch(ctypes.byref(d), None, *([None] * 9)) == sv.SSM_ERR_NULL
