@@ -14,7 +14,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SRCS = [os.path.join(HERE, "csrc", n) for n in ("ssmverify.cu", "accept.cu")]
+SRCS = [os.path.join(HERE, "csrc", n) for n in ("ssmverify.cu", "accept.cu", "hostcopy.cu")]
 HDRS = [os.path.join(ROOT, "include", "ssmverify.h"), os.path.join(HERE, "csrc", "ssm_internal.h")]
 LIB = os.path.join(HERE, "libssmverify.so")
 

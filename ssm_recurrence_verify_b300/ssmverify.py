@@ -40,7 +40,7 @@ SSM_PREFILL_SCRATCH_BYTES = 64 << 20
 EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
            "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool", "ssm_step_pool",
            "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_scratch", "ssm_selftest_wait_timeout", "ssm_accept_greedy",
-           "ssm_accept_sample", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
+           "ssm_accept_sample", "ssm_copy_from_host", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
 
 
 class SsmDesc(ctypes.Structure):
@@ -96,12 +96,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_step_pool.argtypes = [dp, pp] + [vp] * 9
     lib.ssm_prefill.argtypes = [dp, pp] + [vp] * 8 + [ctypes.c_int64, vp, vp]
     lib.ssm_prefill_scratch.argtypes = [dp, pp] + [vp] * 9
+    lib.ssm_copy_from_host.argtypes = [vp, vp, ctypes.c_int64, vp]
     lib.ssm_prefill_workspace_bytes.argtypes = [dp]
     lib.ssm_prefill_workspace_bytes.restype = ctypes.c_int64
     for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
               "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool",
               "ssm_step_pool", "ssm_prefill", "ssm_prefill_scratch", "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample",
-              "ssm_last_cuda_error", "ssm_version"):
+              "ssm_copy_from_host", "ssm_last_cuda_error", "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
     lib.ssm_strerror.restype = ctypes.c_char_p
@@ -443,3 +444,17 @@ def prefill_scratch(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, st
     _check(load_library().ssm_prefill_scratch(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
                                               _ptr(dt), _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
+
+
+def copy_from_host(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """dst <- src, from a page-locked host tensor to a CUDA tensor of the same
+    size, with the SMs reading the host memory (asynchronous on the stream)."""
+    if dst.numel() * dst.element_size() != src.numel() * src.element_size():
+        raise ValueError("dst and src must have the same number of bytes")
+    if not dst.is_cuda or src.is_cuda or not src.is_pinned():
+        raise ValueError("dst must be a CUDA tensor and src a page-locked (pinned) host tensor")
+    if not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("dst and src must be contiguous")
+    _check(load_library().ssm_copy_from_host(_ptr(dst), _ptr(src), dst.numel() * dst.element_size(),
+                                             _stream(stream)))
+    return dst

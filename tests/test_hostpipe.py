@@ -69,3 +69,30 @@ def test_captured_step_equals_device_calls(cuda_device):
             torch.cuda.synchronize()
             assert torch.equal(h["y"], y_ref.cpu()), (rnd, layer)
             assert torch.equal(pipes[layer].state, st_ref), (rnd, layer)
+
+
+@pytest.mark.parametrize("nbytes,offset", [(1, 0), (15, 0), (16, 0), (4096 + 7, 0), (6 << 20, 0), (100003, 3)])
+def test_copy_from_host(cuda_device, nbytes, offset):
+    """SM-driven copies from page-locked memory: exact bytes for aligned and
+    unaligned ranges with ragged tails."""
+    from ssm_recurrence_verify_b300 import ssmverify as sv
+    g = torch.Generator().manual_seed(nbytes)
+    h = torch.randint(0, 256, (nbytes + offset,), dtype=torch.uint8, generator=g).pin_memory()
+    d = torch.full((nbytes + offset,), 7, dtype=torch.uint8, device=cuda_device)
+    sv.copy_from_host(d[offset:], h[offset:])
+    torch.cuda.synchronize()
+    assert torch.equal(d[offset:].cpu(), h[offset:])
+    if offset:
+        assert (d[:offset] == 7).all()
+
+
+def test_copy_from_host_refuses_pageable_memory(cuda_device):
+    from ssm_recurrence_verify_b300 import ssmverify as sv
+    h = torch.zeros(64, dtype=torch.uint8)  # not page-locked
+    d = torch.empty(64, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(ValueError):
+        sv.copy_from_host(d, h)
+    lib = sv.load_library()
+    import ctypes
+    rc = lib.ssm_copy_from_host(ctypes.c_void_p(d.data_ptr()), ctypes.c_void_p(h.data_ptr()), 64, None)
+    assert rc == sv.SSM_ERR_UNSUPPORTED
