@@ -18,7 +18,7 @@
 //
 // Kernel design (B300; bound by the HBM stream of the logits it must read):
 //  * One thread-block cluster of kCl CTAs per sequence; CTA r owns a slice
-//    of V / kCl vocabulary entries of every row and streams it with 16-byte
+//    of V / kCl vocabulary entries of each row it reads and streams it with 16-byte
 //    loads, kAU of them in flight per thread.
 //  * The rule only ever looks at rows up to the first rejection, so the
 //    rows are read in steps of kGroup draft tokens (their verifier rows and,
@@ -551,7 +551,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
         return;
     }
 
-    // ---- phase 4 (sampling): the next token, by inverse CDF at u_K
+    // ---- the draw (sampling): the next token, by inverse CDF at u_K over row j
     Weigher wf;
     wf.resid = j < K && !badj;
     {
