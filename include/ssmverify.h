@@ -40,10 +40,10 @@
  * between calls is a cache of immutable device properties (SM count and
  * resident blocks per SM, per kernel and device), so calls are thread-safe
  * (ssm_prefill_scratch alone also uses a fixed device array; see there).
- * Every entry point only validates its arguments and enqueues one kernel (ssm_prefill: up to three;
- * ssm_copy_from_host: a copy kernel) on
- * `stream` (a cudaStream_t passed as void*, NULL = the legacy default
- * stream) on the current device. Calls are asynchronous.
+ * Every entry point only validates its arguments and enqueues one kernel
+ * (ssm_prefill: up to three) on `stream` (a cudaStream_t passed as void*,
+ * NULL = the legacy default stream) on the current device. Calls are
+ * asynchronous. ssm_copy_from_host alone takes a host pointer (its source).
  *
  * Errors: the return value is SSM_OK or an SSM_ERR_* code. Argument errors
  * are detected on the host before anything is launched (no device work is
