@@ -34,12 +34,20 @@
 //    no split. The state stays in registers in the mma fragment layout: warp
 //    w owns 16 rows of the tile, a thread rows g and g + 8 and, of each 8
 //    columns, those the fragment gives it.
-//  * The state itself advances by the exact recurrence (h <- Abar h + u B,
-//    two IEEE roundings per element, paired fp32 instructions) only as far
-//    as needed: up to the committed token j (and through the chunk when
-//    more chunks follow). Every flavour shares that device function, so the
-//    fused, commit-only, deferred-commit and single-step paths agree bit for
-//    bit, and verify-only launches run no recurrence at all for K <= kTC.
+//  * The state advances only as far as needed: up to the committed token j
+//    (and through the chunk when more chunks follow); verify-only launches
+//    do not advance it at all for K <= kTC. At N <= 128 the advance over the
+//    first m tokens of a chunk is the recurrence regrouped into one rank-8
+//    tensor-core product,
+//        h <- lambda h + sum_{s<m} w_s u_s B_s^T,  lambda = prod_{s<m} Abar_s,
+//        w_s = prod_{s<r<m} Abar_r,
+//    formed from zero and added to lambda h by one fp32 fma per element
+//    (round to nearest), with the register state as the mma D fragment. The
+//    committed state is always formed by that same arithmetic over the same
+//    tokens, so the fused, commit-only and deferred-commit paths, and a
+//    block that ends at the committed token, write it bit for bit alike. At
+//    N = 256 (two warps per band) the state takes the exact recurrence
+//    h <- Abar h + u B token by token (paired fp32 instructions).
 //  * Flavours: a replay phase (advance over the accepted prefix of a replay
 //    block, write h_j) and/or a verify phase (y for every draft token; the
 //    fused flavour writes h_j, j = accept_len, straight from registers).
@@ -71,7 +79,6 @@ enum Flavour : int {
 // (a pool), and every tile starts from h = 0 without reading a state.
 constexpr int kPoolBit = 8;
 constexpr int kZeroBit = 16;
-constexpr int kMmaBit = 32;  // verify phase: the state crosses full chunks on the tensor cores (N <= 128)
 
 template <int F>
 struct Flav {
@@ -81,7 +88,6 @@ struct Flav {
     static constexpr bool kWriteInVerify = kBase == kVerifyCommit;
     static constexpr bool kPool = (F & kPoolBit) != 0;
     static constexpr bool kZero = (F & kZeroBit) != 0;
-    static constexpr bool kMmaAdvance = (F & kMmaBit) != 0;
 };
 
 // Per-N geometry. A band is 16 rows (one mma M block); WPB warps share a
@@ -429,8 +435,8 @@ __device__ __forceinline__ ChunkDt load_chunk_dt(const Args &a, const Block &blk
 // Convert one chunk of tc tokens into the staged fp32 arrays, from the raw
 // rows in shared memory (FROM_RAW: offsets rawX / rawB / rawC) or from global
 // memory. x items are 8 rows of one token (u = dt x and D x), B/C items 8
-// columns of one token. Tokens tc .. kTC-1 of u are zeroed (they meet zero
-// weights in the intra-chunk contraction and must not be NaN). Warp 0 also
+// columns of one token. Tokens tc .. kTC-1 of u and B are zeroed (they meet
+// zero weights in the contractions over the chunk and must not be NaN). Warp 0 also
 // forms Abar, cs_t = sum_{r<=t} dt_r and w_t = exp(A cs_t) (verify phase).
 template <typename Tin, int N, bool WANT_Y, bool FROM_RAW>
 __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, const Tile &T, int t0, int tc, float Ah,
@@ -476,12 +482,19 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
         }
     }
     // B / C items: 8 columns = two 4-column chunks, each to its thread's slots.
+    // B of tokens tc .. kTC-1 is zeroed (the state update contracts over all
+    // kTC tokens with zero weights there).
 #pragma unroll 1
-    for (int i = tid; i < tc * BPT; i += kThreads) {
+    for (int i = tid; i < kTC * BPT; i += kThreads) {
         const int t = i / BPT, n8 = i % BPT;
         const long long off = ((bt0 + t) * a.G + T.g) * N + 8 * n8;
         const int tb = t * Geo<N>::kWPB * 4 * Geo<N>::kPad;
         const int p0 = tb + perm_index<N>(8 * n8), p1 = tb + perm_index<N>(8 * n8 + 4);
+        if (t >= tc) {
+            st4(sm<float>(so.B) + p0, 0.f, 0.f, 0.f, 0.f);
+            st4(sm<float>(so.B) + p1, 0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
         Raw8<Tin> r;
         float v[8];
         if (FROM_RAW) lds8(sm<const Tin>(rawB) + t * N + 8 * n8, r);
@@ -609,63 +622,105 @@ __device__ __forceinline__ Split split(float x) {
     return s;
 }
 
-// Advance the register state over the staged chunk (tc tokens) on the tensor
-// cores -- the recurrence regrouped over the chunk:
-//     h <- lambda h + sum_s w_s u_s B_s^T,   lambda = prod_s Abar_s,   w_s = prod_{r > s} Abar_r
-// as one rank-8 update, mma.sync m16n8k8 tf32 with the state itself as the
-// accumulator. The thread's slot pair (2 nb, 2 nb + 1) of rows g and g + 8 is
-// the D fragment of n-block nb under the column permutation of the staged B
-// (logical column j of n-block nb is physical column
-// 4 (j / 2) + 16 (nb / 2) + 2 (nb % 2) + j % 2, staged at row j / 2, slot
-// 2 nb + j % 2), so no state moves. w o u is split into tf32 high and low
-// parts; bf16 B is exact in tf32, fp32 B is split as well. Layouts with one
-// warp per band (N <= 128) only.
+// The state crossing staged tokens [0, tc) of a chunk, regrouped (the recurrence
+// unrolled over the tokens):
+//     h <- lambda h + sum_{s<tc} w_s u_s B_s^T,   lambda = prod_{s<tc} Abar_s,   w_s = prod_{s<r<tc} Abar_r.
+// This thread's A-fragment tokens are tq and tq + 4 (w = 0 from tc on).
+struct AdvW {
+    float w0, w1, lam;
+};
+__device__ __forceinline__ AdvW adv_weights(const float *abar, int tq, int tc) {
+    AdvW r{0.f, 0.f, 1.f};
+#pragma unroll
+    for (int t = kTC - 1; t >= 0; --t) {
+        if (t < tc) {
+            if (t == tq) r.w0 = r.lam;
+            if (t == tq + 4) r.w1 = r.lam;
+            r.lam = __fmul_rn(r.lam, abar[t]);
+        }
+    }
+    return r;
+}
+
+// A fragment of w o u (rows g, g + 8 of the band; tokens tq, tq + 4), split
+// into tf32 high and low parts.
+struct AFrag {
+    Split a0, a1, a2, a3;
+};
+template <int ROWS>
+__device__ __forceinline__ AFrag adv_frag(const float *U, const Lane &L, const AdvW &w) {
+    const int r0 = L.band * 16 + L.g, r1 = r0 + 8, t0 = L.tq, t1 = L.tq + 4;
+    return AFrag{split(__fmul_rn(w.w0, U[t0 * ROWS + r0])), split(__fmul_rn(w.w0, U[t0 * ROWS + r1])),
+                 split(__fmul_rn(w.w1, U[t1 * ROWS + r0])), split(__fmul_rn(w.w1, U[t1 * ROWS + r1]))};
+}
+
+// The rank-tc term of one n-block, sum_s w_s u_s B_s^T, from zero (small
+// parts first); bf16 B is exact in tf32, fp32 B is split as well.
+template <typename Tin>
+__device__ __forceinline__ void rank_term(float (&d)[4], const AFrag &a, float b0, float b1) {
+    d[0] = d[1] = d[2] = d[3] = 0.f;
+    if constexpr (sizeof(Tin) == 2) {
+        mma_tf32(d, a.a0.lo, a.a1.lo, a.a2.lo, a.a3.lo, __float_as_uint(b0), __float_as_uint(b1));
+        mma_tf32(d, a.a0.hi, a.a1.hi, a.a2.hi, a.a3.hi, __float_as_uint(b0), __float_as_uint(b1));
+    } else {
+        const Split c0 = split(b0), c1 = split(b1);
+        mma_tf32(d, a.a0.lo, a.a1.lo, a.a2.lo, a.a3.lo, c0.hi, c1.hi);
+        mma_tf32(d, a.a0.hi, a.a1.hi, a.a2.hi, a.a3.hi, c0.lo, c1.lo);
+        mma_tf32(d, a.a0.hi, a.a1.hi, a.a2.hi, a.a3.hi, c0.hi, c1.hi);
+    }
+}
+
+// Advance the register state over staged tokens [0, tc) on the tensor cores:
+// one rank-8 mma.sync m16n8k8 tf32 product per n-block, then h <- lambda h +
+// term (one fp32 fma, round to nearest). The thread's slot pair (2 nb,
+// 2 nb + 1) of rows g and g + 8 is the D fragment of n-block nb under the
+// column permutation of the staged B (logical column j of n-block nb is
+// physical column 4 (j / 2) + 16 (nb / 2) + 2 (nb % 2) + j % 2, staged at row
+// j / 2, slot 2 nb + j % 2), so no state moves. One warp per band (N <= 128).
 template <typename Tin, int N>
 __device__ __forceinline__ void advance_mma(float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L, const StagedOffsets &so,
                                             int tc) {
     using G = Geo<N>;
     static_assert(G::kWPB == 1, "one warp per band");
-    constexpr int ROWS = G::kRows;
-    const float *abar = sm<const float>(so.Abar);
-    const int t0 = L.tq, t1 = L.tq + 4;  // this thread's two tokens of the A fragment
-    float w0 = 0.f, w1 = 0.f, lam = 1.f;  // w = 0 past tc (u is zero there too)
-#pragma unroll
-    for (int t = kTC - 1; t >= 0; --t) {
-        if (t < tc) {
-            if (t == t0) w0 = lam;
-            if (t == t1) w1 = lam;
-            lam = __fmul_rn(lam, abar[t]);
-        }
-    }
-    const float2 l2 = make_float2(lam, lam);
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int m = 0; m < G::kNC / 2; ++m) hs[rr][m] = __fmul2_rn(hs[rr][m], l2);
-    const float *U = sm<const float>(so.U);
-    const int r0 = L.band * 16 + L.g, r1 = r0 + 8;
-    const Split a0 = split(__fmul_rn(w0, U[t0 * ROWS + r0]));
-    const Split a1 = split(__fmul_rn(w0, U[t0 * ROWS + r1]));
-    const Split a2 = split(__fmul_rn(w1, U[t1 * ROWS + r0]));
-    const Split a3 = split(__fmul_rn(w1, U[t1 * ROWS + r1]));
-    const float *Bs = sm<const float>(so.B);
-    const int col = (L.g >> 1) * G::kPad + (L.g & 1);
-    const float *b0p = Bs + t0 * 4 * G::kPad + col, *b1p = Bs + t1 * 4 * G::kPad + col;
+    const AdvW w = adv_weights(sm<const float>(so.Abar), L.tq, tc);
+    const AFrag a = adv_frag<G::kRows>(sm<const float>(so.U), L, w);
+    const float2 l2 = make_float2(w.lam, w.lam);
+    const float *Bs = sm<const float>(so.B) + (L.g >> 1) * G::kPad + (L.g & 1);
+    const float *b0p = Bs + L.tq * 4 * G::kPad, *b1p = Bs + (L.tq + 4) * 4 * G::kPad;
 #pragma unroll
     for (int nb = 0; nb < G::kNC / 2; ++nb) {
-        const float b0 = b0p[2 * nb], b1 = b1p[2 * nb];
-        float d[4] = {hs[0][nb].x, hs[0][nb].y, hs[1][nb].x, hs[1][nb].y};
-        if constexpr (sizeof(Tin) == 2) {
-            mma_tf32(d, a0.hi, a1.hi, a2.hi, a3.hi, __float_as_uint(b0), __float_as_uint(b1));
-            mma_tf32(d, a0.lo, a1.lo, a2.lo, a3.lo, __float_as_uint(b0), __float_as_uint(b1));
-        } else {
-            const Split c0 = split(b0), c1 = split(b1);
-            mma_tf32(d, a0.hi, a1.hi, a2.hi, a3.hi, c0.hi, c1.hi);
-            mma_tf32(d, a0.lo, a1.lo, a2.lo, a3.lo, c0.hi, c1.hi);
-            mma_tf32(d, a0.hi, a1.hi, a2.hi, a3.hi, c0.lo, c1.lo);
-        }
-        hs[0][nb] = make_float2(d[0], d[1]);
-        hs[1][nb] = make_float2(d[2], d[3]);
+        float d[4];
+        rank_term<Tin>(d, a, b0p[2 * nb], b1p[2 * nb]);
+        hs[0][nb] = __ffma2_rn(l2, hs[0][nb], make_float2(d[0], d[1]));
+        hs[1][nb] = __ffma2_rn(l2, hs[1][nb], make_float2(d[2], d[3]));
+    }
+}
+
+// The state after token jc - 1 of the staged chunk, written to global memory
+// without changing the register state: each n-block's value is formed by
+// exactly the arithmetic of advance_mma(jc), so the written state equals that
+// of a block that ends at that token. `sl` = state + sbase + row0 * N.
+template <typename Tin, int N>
+__device__ __forceinline__ void commit_mma(const float2 (&hs)[2][Geo<N>::kNC / 2], const Lane &L,
+                                           const StagedOffsets &so, int jc, float *sl, int rows) {
+    using G = Geo<N>;
+    static_assert(G::kWPB == 1, "one warp per band");
+    const AdvW w = adv_weights(sm<const float>(so.Abar), L.tq, jc);
+    const AFrag a = adv_frag<G::kRows>(sm<const float>(so.U), L, w);
+    const float2 l2 = make_float2(w.lam, w.lam);
+    const float *Bs = sm<const float>(so.B) + (L.g >> 1) * G::kPad + (L.g & 1);
+    const float *b0p = Bs + L.tq * 4 * G::kPad, *b1p = Bs + (L.tq + 4) * 4 * G::kPad;
+    const int r0 = L.band * 16 + L.g;
+    float *row0 = sl + (long long)r0 * N + L.half * G::kNCW + 4 * L.tq, *row1 = row0 + 8LL * N;
+#pragma unroll
+    for (int nb = 0; nb < G::kNC / 2; ++nb) {
+        float d[4];
+        rank_term<Tin>(d, a, b0p[2 * nb], b1p[2 * nb]);
+        // slot pair nb of rows g and g + 8: columns 4 (tq + 4 (nb / 2)) + 2 (nb % 2) + {0, 1}
+        const int off = 16 * (nb >> 1) + 2 * (nb & 1);
+        if (r0 < rows) __stcs(reinterpret_cast<float2 *>(row0 + off), __ffma2_rn(l2, hs[0][nb], make_float2(d[0], d[1])));
+        if (r0 + 8 < rows)
+            __stcs(reinterpret_cast<float2 *>(row1 + off), __ffma2_rn(l2, hs[1][nb], make_float2(d[2], d[3])));
     }
 }
 
@@ -977,8 +1032,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
                     stage_chunk<Tin, N, false, false>(a, a.rep, T, t0, tc, Ah, 0.f, sR, 0, 0, 0, d);
                     __syncthreads();
                 }
+                if constexpr (G::kWPB == 1) {
+                    advance_mma<Tin, N>(hs, L, sR, tc);
+                } else {
 #pragma unroll 1
-                for (int s = 0; s < tc; ++s) recur_token<N>(hs, L, sR, s);
+                    for (int s = 0; s < tc; ++s) recur_token<N>(hs, L, sR, s);
+                }
             }
             if (jr > 0) store_state<N>(hs, L, sl, T.rows);
         }
@@ -998,19 +1057,27 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
                 chunk_y<Tin, N>(hs, L, sV, tc, Ah, ytile + t0 * ystride, ystride, T.rows);
                 // Advance the state by the recurrence as far as it is needed: through the
                 // chunk when more chunks follow, else up to the committed token.
-                int steps = 0;
-                if (t0 + tc < K) steps = tc;
-                else if (FL::kWriteInVerify && jw >= t0) steps = jw - t0 + 1;
-                if constexpr (FL::kMmaAdvance && G::kWPB == 1) {
-                    if (t0 + tc < K) {  // the next chunk starts from h after this one: no state is written here
+                const bool more = t0 + tc < K;
+                if constexpr (G::kWPB == 1) {
+                    // jc: the committed state is the one after token jc - 1 of this chunk
+                    const int jc = (FL::kWriteInVerify && jw >= t0 && jw < t0 + tc) ? jw - t0 + 1 : 0;
+                    if (more && jc > 0 && jc < tc) {
+                        commit_mma<Tin, N>(hs, L, sV, jc, sl, T.rows);
                         advance_mma<Tin, N>(hs, L, sV, tc);
-                        steps = 0;
+                    } else {
+                        const int adv = more ? tc : jc;
+                        if (adv > 0) advance_mma<Tin, N>(hs, L, sV, adv);
+                        if (jc > 0) store_state<N>(hs, L, sl, T.rows);
                     }
-                }
+                } else {
+                    int steps = 0;
+                    if (more) steps = tc;
+                    else if (FL::kWriteInVerify && jw >= t0) steps = jw - t0 + 1;
 #pragma unroll 1
-                for (int s = 0; s < steps; ++s) {
-                    recur_token<N>(hs, L, sV, s);
-                    if (FL::kWriteInVerify && t0 + s == jw) store_state<N>(hs, L, sl, T.rows);
+                    for (int s = 0; s < steps; ++s) {
+                        recur_token<N>(hs, L, sV, s);
+                        if (FL::kWriteInVerify && t0 + s == jw) store_state<N>(hs, L, sl, T.rows);
+                    }
                 }
             }
         }
@@ -1377,7 +1444,6 @@ struct Call {
     int nslots = 0;
     bool zero_state = false;        // internal: every tile starts from h = 0, nothing is read
     bool accept_all = false;        // internal: the replay block is replayed in full (no accept_len)
-    bool mma_advance = false;       // internal (verify, N <= 128): full chunks crossed on the tensor cores
 };
 
 // Validate everything on the host, then launch (with dry: validate only).
@@ -1484,8 +1550,7 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    const int FX = F | (c.pool ? kPoolBit : 0) | (c.zero_state ? kZeroBit : 0) |
-                   (c.mma_advance && d->dstate <= 128 ? kMmaBit : 0);
+    const int FX = F | (c.pool ? kPoolBit : 0) | (c.zero_state ? kZeroBit : 0);
     switch (FX) {
         case kVerify: e = launch_flavour<kVerify>(d->in_dtype, N, a, s); break;
         case kCommit: e = launch_flavour<kCommit>(d->in_dtype, N, a, s); break;
@@ -1496,8 +1561,6 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
         case kCommitVerify | kPoolBit: e = launch_flavour<kCommitVerify | kPoolBit>(d->in_dtype, N, a, s); break;
         case kVerifyCommit | kPoolBit: e = launch_flavour<kVerifyCommit | kPoolBit>(d->in_dtype, N, a, s); break;
         case kCommit | kZeroBit: e = launch_flavour<kCommit | kZeroBit>(d->in_dtype, N, a, s); break;
-        case kVerify | kMmaBit: e = launch_flavour<kVerify | kMmaBit>(d->in_dtype, N, a, s); break;
-        case kVerify | kPoolBit | kMmaBit: e = launch_flavour<kVerify | kPoolBit | kMmaBit>(d->in_dtype, N, a, s); break;
         default: return SSM_ERR_UNSUPPORTED;  // no kernel for this combination
     }
     if (e != cudaSuccess) {
@@ -1692,7 +1755,6 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     Call c3{};
     c3.flavour = kVerify;
     c3.state_in = static_cast<const float *>(ws);
-    c3.mma_advance = true;
     if (vslot != nullptr) {  // chunks of sequences without a valid slot write no y
         c3.pool = true;
         c3.slot = vslot;

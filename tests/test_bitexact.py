@@ -3,19 +3,23 @@
 The accepted-prefix selection must be exact: the state committed by the fused
 kernel after K drafted tokens with j accepted is, bit for bit, the state of
   * ssm_commit with the same j,
-  * j plain single-token steps,
   * a fused run drafting only the j accepted tokens,
 and j = 0 leaves the cached state bitwise unchanged. y does not depend on the
-entry point (verify and verify_commit) nor on j.
+entry point (verify and verify_commit) nor on j. j plain single-token steps
+reach the same state up to fp32 rounding: at N <= 128 the kernels advance the
+state by one rank-m tensor-core update over the m tokens of a chunk, and m
+rank-1 updates round differently.
 """
 import pytest
 import torch
 
 import ssm_recurrence_verify_b300 as ssm
-from gpu_helpers import to_dev
+from gpu_helpers import np64, rel_err, to_dev
 from ssm_recurrence_verify_b300 import synth
 
 pytestmark = pytest.mark.gpu
+
+STEP_RTOL = 1e-5  # j rank-1 updates against one rank-j update: a few fp32 roundings per element
 
 CASES = [
     (8, 4, 128, 128, 2, 8, synth.BF16),
@@ -57,7 +61,10 @@ def test_fused_commit_step_agree(cuda_device, case):
             ssm.step(s_step, d["x"][b:b + 1, t:t + 1].contiguous(), d["B"][b:b + 1, t:t + 1].contiguous(),
                      d["C"][b:b + 1, t:t + 1].contiguous(), d["dt"][b:b + 1, t:t + 1].contiguous(), d["A"], d["D"])
         torch.cuda.synchronize()
-        assert torch.equal(s_step[0], s_fused[b]), (b, j)
+        if case[3] > 128:  # token-by-token recurrence in every entry point
+            assert torch.equal(s_step[0], s_fused[b]), (b, j)
+        else:
+            assert rel_err(np64(s_step[0]), np64(s_fused[b])) <= STEP_RTOL, (b, j)
         if j == 0:
             assert torch.equal(s_fused[b], d["state0"][b])
         else:

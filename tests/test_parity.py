@@ -221,3 +221,32 @@ def test_commit_verify_varying_draft_length(cuda_device):
     def wl_of(r):
         return synth.custom_workload(3, 4, 50, 64, 2, ks[r], synth.F32, seed=32)
     _serving_rounds(cuda_device, wl_of, len(ks), bad_round=2)
+
+
+@pytest.mark.parametrize("K", [1, 8])
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_long_decode_slow_decay(cuda_device, K, dtype):
+    """2048 tokens through one cached state with decays near 1 (A from -0.1
+    down to 0, where the state is a plain running sum), as token-by-token
+    steps (K = 1) or as rounds of 8 fully accepted drafts, against the fp64
+    oracle over the whole sequence: the rounding of the state update must not
+    drift past the state tolerance over a long decode."""
+    dev = cuda_device
+    T = 2048
+    wl = synth.custom_workload(2, 4, 64, 128, 2, T, dtype, seed=77)
+    d = synth.draw_layer_round(wl)
+    d["A"] = torch.tensor([-0.1, -1e-2, -1e-3, 0.0], dtype=torch.float32)
+    ref = oracle.verify_commit(d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], None)
+    dd = to_dev(d, dev)
+    st = dd["state0"].clone()
+    full = torch.full((2,), K, dtype=torch.int32, device=dev)
+    ys = []
+    for t0 in range(0, T, K):
+        blk = [dd[k][:, t0:t0 + K].contiguous() for k in ("x", "B", "C", "dt")]
+        if K == 1:
+            ys.append(ssm.step(st, *blk, dd["A"], dd["D"]))
+        else:
+            ys.append(ssm.verify_commit(st, *blk, dd["A"], dd["D"], full))
+    y = torch.cat(ys, dim=1)
+    torch.cuda.synchronize()
+    _check(y, st, ref, wl.torch_in_dtype, f"long decode K={K}")
