@@ -4,8 +4,10 @@ bandwidth of the fused verify/commit kernel against the B300 roofline.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 3] [--cpu-seconds 10] [--no-cpu-baseline]
 
-A step is one pass of the whole path over one batch: for every layer of the
-workload one fused verify+commit launch (plain decode: one step launch).
+A step is one pass of the whole path over one batch: every layer of the
+workload through the fused verify+commit (plain decode: the step), as one
+launch over the layer stack (nlayers) or, with --per-layer-launches, one
+launch per layer. The value counts draft tokens x layers per second.
 The default workload is the batched speculative-serving load (64 sequences,
 one Llama-3-8B-shaped layer: H 32, P 128, N 128, G 8, K 8, bf16 inputs, fp32
 state). Inputs are seeded synthetic data drawn on the CPU and resident in HBM
@@ -243,21 +245,31 @@ def recorded_traffic(workload_name: str):
 # ----------------------------------------------------------------------------- GPU arm
 
 class LayerSet:
-    """One independent input set: per layer the state, inputs, y and status."""
+    """One independent input set of a round: the layer stack's state, inputs,
+    y and status as [L]-leading slabs (`stack`; accept_len [batch] is shared
+    by the layers), and per layer views of them (`layers`)."""
 
     def __init__(self, wl, batch, offset, rnd, dev, layers):
+        ds = [synth.draw_layer_round(wl, rnd=rnd, layer=layer, batch=batch, batch_offset=offset)
+              for layer in range(layers)]
+        self.stack = {k: torch.stack([d[k] for d in ds]).to(dev) for k in ("state0", "x", "B", "C", "dt", "A", "D")}
+        self.stack["accept_len"] = ds[0]["accept_len"].to(dev)  # one accepted prefix per sequence, every layer
+        self.stack["y"] = torch.empty((layers, batch, wl.ntok, wl.nheads, wl.headdim), dtype=torch.float32,
+                                      device=dev)
+        self.stack["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
         self.layers = []
-        for layer in range(layers):
-            d = synth.draw_layer_round(wl, rnd=rnd, layer=layer, batch=batch, batch_offset=offset)
-            e = {k: v.to(dev) for k, v in d.items()}
-            e["y"] = torch.empty((batch, wl.ntok, wl.nheads, wl.headdim), dtype=torch.float32, device=dev)
-            e["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+        for layer, d in enumerate(ds):
+            e = {k: self.stack[k][layer] for k in ("state0", "x", "B", "C", "dt", "A", "D", "y")}
+            e["accept_len"] = self.stack["accept_len"]
+            e["status"] = self.stack["status"]
             e["host"] = d
             e["accepted_nonzero"] = int((d["accept_len"] > 0).sum())
             self.layers.append(e)
 
 
 def launch_layer(ssm, wl, e):
+    """One layer-call (per-layer tensors), or one call over the whole stack
+    (the [L]-leading slabs of LayerSet.stack)."""
     if wl.accept == "all" and wl.ntok == 1:
         ssm.step(e["state0"], e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], y=e["y"])
     else:
@@ -280,11 +292,14 @@ def run_ours(args, wl, rank, world, local_rank):
     sets = [LayerSet(wl, batch, offset, rnd, dev, nl) for rnd in range(nsets)]
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
+    # a layer stack runs as one launch per step (nlayers = L), unless asked per layer
+    per_step = 1 if (nl > 1 and not args.per_layer_launches) else nl
+    units = (lambda s: [s.stack]) if per_step == 1 and nl > 1 else (lambda s: s.layers)
 
     # eager warm-up of every set
     with torch.cuda.stream(stream):
         for s in sets:
-            for e in s.layers:
+            for e in units(s):
                 launch_layer(ssm, wl, e)
     torch.cuda.synchronize()
 
@@ -292,13 +307,13 @@ def run_ours(args, wl, rank, world, local_rank):
     # (step i uses input set i mod nsets; at most MAX_GRAPH_LAUNCHES launches
     # per graph) and replayed back to back, as a serving loop runs its layers.
     def capture(step_sets):
-        per = max(1, MAX_GRAPH_LAUNCHES // nl)
+        per = max(1, MAX_GRAPH_LAUNCHES // per_step)
         out = []
         for i in range(0, len(step_sets), per):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for si in step_sets[i:i + per]:
-                    for e in sets[si].layers:
+                    for e in units(sets[si]):
                         launch_layer(ssm, wl, e)
             out.append(g)
         return out
@@ -337,11 +352,12 @@ def run_ours(args, wl, rank, world, local_rank):
     # per-step algorithmic bytes, averaged over the sets the timed steps used
     step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
     used = [step_bytes[si] for si in timed_sets]
-    mean_launch_bytes = statistics.fmean(used) / nl
-    mean_launch_ms = elapsed_ms / (K * nl)  # this rank's average launch duration over the timed region
+    mean_launch_bytes = statistics.fmean(used) / per_step
+    mean_launch_ms = elapsed_ms / (K * per_step)  # this rank's average launch duration over the timed region
     achieved = mean_launch_bytes / (mean_launch_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    tokens_per_step = batch * wl.ntok * world  # per layer: every rank's sequences x draft tokens
+    # per SSM layer: Bsz K / t_layer, i.e. every rank's sequences x draft tokens x layers per step time
+    tokens_per_step = batch * wl.ntok * world * nl
     value = tokens_per_step * K / (max_ms * 1e-3)
 
     e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 else None
@@ -349,8 +365,8 @@ def run_ours(args, wl, rank, world, local_rank):
         "value": value, "ms_per_step": max_ms / K, "elapsed_ms": max_ms, "wall_s": wall1 - wall0,
         "launch_ms_mean": mean_launch_ms, "graphs": len(timed_graphs),
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "bytes_per_launch": mean_launch_bytes,
-        "clocks": sampler.summary(wall0, wall1), "nsets": nsets, "e2e": e2e, "launches": K * nl,
-        "batch": batch,
+        "clocks": sampler.summary(wall0, wall1), "nsets": nsets, "e2e": e2e, "launches": K * per_step,
+        "batch": batch, "layers_per_launch": nl // per_step,
     }
 
 
@@ -399,7 +415,7 @@ def run_e2e(ssm, args, wl, s, stream, dev, world):
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     for p in pipes:
         assert int(p.status.item()) == 0, "device reported a bad accept_len"
-    return {"value": s.layers[0]["x"].shape[0] * wl.ntok * world * n / (ms * 1e-3), "unit": "tokens/s",
+    return {"value": s.layers[0]["x"].shape[0] * wl.ntok * len(s.layers) * world * n / (ms * 1e-3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "path": f"HostPipeline: {chunks} sequence chunks per layer, copy-in (SM reads of pinned memory) / "
                     f"kernel / copy-out streams overlapped, {per_graph} consecutive steps per CUDA graph"}
@@ -743,6 +759,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--per-layer-launches", action="store_true",
+                    help="run a layer stack as one launch per layer instead of one launch over all layers")
     ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill"], default="ssm",
                     help="ssm: the verify/commit step (default); accept_*: the acceptance step alone; "
                          "prefill: a 2048-token prompt through one layer")
@@ -782,7 +800,7 @@ def main(argv=None):
             "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
-            "config": workload_config(wl, r["nsets"]),
+            "config": dict(workload_config(wl, r["nsets"]), layers_per_launch=r["layers_per_launch"]),
             "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": r["peak"], "unit": "GB/s",
                          "frac": r["achieved_gbs"] / r["peak"], "traffic": traffic,
                          "peak_source": f"{r['peak_kind']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",

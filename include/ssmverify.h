@@ -105,8 +105,24 @@ typedef struct {
     int32_t ngroups;  /* G: B/C groups; head h uses group h / (H / G) */
     int32_t ntok;     /* K: draft tokens per sequence */
     int32_t in_dtype; /* SSM_F32 or SSM_BF16 for x, B, C, dt */
-    int32_t reserved; /* must be 0 */
+    int32_t nlayers;  /* layers in one call: 0 or 1 = one layer (the layouts above); L > 1: a layer stack */
 } ssm_desc_t;
+
+/*
+ * Layer stacks (desc->nlayers = L > 1; ssm_verify, ssm_commit,
+ * ssm_verify_commit, ssm_commit_verify and ssm_step). A hybrid model runs the
+ * same K draft tokens through every Mamba layer, each layer with its own
+ * cached state and its own inputs (the speculative-decoding section: every
+ * Mamba layer of the verifier rolls back to the same last accepted token).
+ * One call then covers all L layers: state, x, B, C, dt, y (and x_prev,
+ * B_prev, dt_prev) carry a leading [L] dimension in front of their layouts
+ * above (state [L][batch][nheads][headdim][dstate], x [L][batch][ntok]
+ * [nheads][headdim], ...), A and D are [L][nheads], and accept_len (and
+ * accept_len_prev) stays [batch]: one accepted prefix per sequence, shared
+ * by every layer. The result equals L single-layer calls on the slices; the
+ * pool entry points and prefill take one layer (L > 1 there:
+ * SSM_ERR_UNSUPPORTED). nlayers < 0: SSM_ERR_SHAPE.
+ */
 
 /*
  * ssm_verify -- run the K draft tokens from the cached state and emit y for

@@ -167,6 +167,7 @@ struct Args {
     float *y;
     uint32_t *dev_status;
     int H, P, G, ptiles;
+    int bpl;  // sequences per layer: a layer stack is one batch of nlayers x bpl sequences
     long long ntiles;
 };
 
@@ -364,7 +365,8 @@ __device__ __forceinline__ int perm_index(int n) {
 // ----------------------------------------------------------------------------- tile context
 
 struct Tile {
-    long long b;
+    long long b;           // sequence of the call (layer-major over a layer stack)
+    int bs, lay;           // sequence within its layer, layer
     int h, g, row0, rows;  // rows: valid rows of this tile (<= kRows)
     long long sbase;       // element offset of the (b, h) state slice
     bool ok;               // the sequence's pool slot is valid (else nothing is written)
@@ -377,7 +379,10 @@ __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, in
     const int ptile = (int)(tt % (uint32_t)a.ptiles);
     const uint32_t bh = tt / (uint32_t)a.ptiles;
     T.h = (int)(bh % (uint32_t)a.H);
-    T.b = (long long)(bh / (uint32_t)a.H);
+    const uint32_t bb = bh / (uint32_t)a.H;
+    T.b = (long long)bb;
+    T.lay = (int)(bb / (uint32_t)a.bpl);
+    T.bs = (int)(bb - (uint32_t)T.lay * (uint32_t)a.bpl);
     T.g = T.h / (a.H / a.G);
     T.row0 = ptile * kRows;
     T.rows = min(kRows, a.P - T.row0);
@@ -826,7 +831,7 @@ __device__ __forceinline__ long long next_work(const Args &a, long long t) {
         if (a.accept_len == nullptr) return t;  // every token of every sequence
         const long long per_b = (long long)a.H * a.ptiles;
         for (; t < a.ntiles; t += gridDim.x) {
-            const int j = __ldg(a.accept_len + t / per_b);
+            const int j = __ldg(a.accept_len + (t / per_b) % a.bpl);  // every layer shares accept_len
             if (j > 0 && j <= a.rep.K) return t;
             if (j != 0 && threadIdx.x == 0 && a.dev_status != nullptr)
                 atomicOr(a.dev_status, SSM_STATUS_BAD_ACCEPT_LEN);
@@ -888,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         Plan pl{nullptr, 0u, 0u, 0u};
         if (tt >= a.ntiles) return pl;
         const Tile T = decode<FL::kPool>(a, tt, ROWS, N);
-        const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.b, a.rep.K), kTC) : 0;
+        const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.bs, a.rep.K), kTC) : 0;
         const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
         const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
         pl.total = (FL::kZero ? 0u : (uint32_t)T.rows * N * 4) + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
@@ -948,10 +953,10 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         TileIn in{0.f, 0.f, 0, -1, {0.f, 0.f}, {0.f, 0.f}};
         if (tt >= a.ntiles) return in;
         const Tile T = decode<FL::kPool>(a, tt, ROWS, N);
-        in.Ah = __ldg(a.A + T.h);
-        if (FL::kVerifyPhase) in.Dh = __ldg(a.D + T.h);
-        if (FL::kReplay) in.jr = accepted(a, T.b, a.rep.K);
-        if (FL::kWriteInVerify) in.jw = accepted(a, T.b, a.ver.K) - 1;
+        in.Ah = __ldg(a.A + T.lay * a.H + T.h);
+        if (FL::kVerifyPhase) in.Dh = __ldg(a.D + T.lay * a.H + T.h);
+        if (FL::kReplay) in.jr = accepted(a, T.bs, a.rep.K);
+        if (FL::kWriteInVerify) in.jw = accepted(a, T.bs, a.ver.K) - 1;
         if constexpr (FL::kReplay) in.dR = load_chunk_dt<Tin, N>(a, a.rep, T, 0, min(in.jr, kTC));
         if constexpr (FL::kVerifyPhase) in.dV = load_chunk_dt<Tin, N>(a, a.ver, T, 0, min(a.ver.K, kTC));
         return in;
@@ -1334,7 +1339,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int check_desc(const ssm_desc_t *d) {
     if (d == nullptr) return SSM_ERR_NULL;
-    if (d->reserved != 0) return SSM_ERR_SHAPE;
+    if (d->nlayers < 0) return SSM_ERR_SHAPE;
     if (d->batch < 0 || d->nheads < 1 || d->headdim < 1 || d->dstate < 1 || d->ngroups < 1 || d->ntok < 1)
         return SSM_ERR_SHAPE;
     if (d->nheads % d->ngroups != 0) return SSM_ERR_SHAPE;
@@ -1457,8 +1462,10 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     if (F == kCommitVerify && rep_K < 1) return SSM_ERR_SHAPE;
     const int N = d->dstate;
     const int ROWS = rows_per_tile(N);
+    const int64_t nl = d->nlayers > 1 ? d->nlayers : 1;  // layers; a stack is nl x batch sequences
+    if (nl > 1 && c.pool) return SSM_ERR_UNSUPPORTED;
     const int64_t ptiles = (d->headdim + ROWS - 1) / ROWS;
-    const int64_t ntiles = (int64_t)d->batch * d->nheads * ptiles;
+    const int64_t ntiles = nl * d->batch * d->nheads * ptiles;
     if (ntiles >= (int64_t)1 << 31) return SSM_ERR_SHAPE;
     if (d->batch == 0) return SSM_OK;
 
@@ -1484,19 +1491,20 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     if (c.accept_len != nullptr && !aligned(c.accept_len, 4)) return SSM_ERR_ALIGN;
     if (c.dev_status != nullptr && !aligned(c.dev_status, 4)) return SSM_ERR_ALIGN;
 
-    const int64_t B_ = d->batch, H = d->nheads, P = d->headdim, G = d->ngroups;
+    // B_: sequences of the call (all layers); accept_len covers one layer's d->batch
+    const int64_t B_ = nl * d->batch, H = d->nheads, P = d->headdim, G = d->ngroups;
     const int64_t state_bytes = (c.pool ? (int64_t)c.nslots : B_) * H * P * N * 4;
     BufList bl;
     if (st != nullptr) bl.add(st, state_bytes, F != kVerify);
     if (c.pool && c.slot != nullptr) bl.add(c.slot, B_ * 4, false);
-    bl.add(c.A, H * 4, false);
+    bl.add(c.A, nl * H * 4, false);
     if (verify_phase) {
         const int64_t bk = B_ * d->ntok;
         bl.add(c.x, bk * H * P * eb, false);
         bl.add(c.B, bk * G * N * eb, false);
         bl.add(c.C, bk * G * N * eb, false);
         bl.add(c.dt, bk * H * eb, false);
-        bl.add(c.D, H * 4, false);
+        bl.add(c.D, nl * H * 4, false);
         bl.add(c.y, bk * H * P * 4, true);
     }
     if (replay && F == kCommitVerify) {  // commit's replay block is the call's x / B / dt, listed below
@@ -1510,7 +1518,7 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
         bl.add(c.Br, bk * G * N * eb, false);
         bl.add(c.dtr, bk * H * eb, false);
     }
-    if (c.accept_len != nullptr) bl.add(c.accept_len, B_ * 4, false);
+    if (c.accept_len != nullptr) bl.add(c.accept_len, (int64_t)d->batch * 4, false);
     if (c.dev_status != nullptr) bl.add(c.dev_status, 4, true);
     if (!bl.disjoint_writes()) return SSM_ERR_ALIAS;
     if (dry) return SSM_OK;
@@ -1546,6 +1554,7 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     a.P = d->headdim;
     a.G = d->ngroups;
     a.ptiles = (int)ptiles;
+    a.bpl = d->batch;
     a.ntiles = ntiles;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1655,6 +1664,7 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
             uint32_t *dev_status, void *stream) {
     int rc = check_desc(d);
     if (rc != SSM_OK) return rc;
+    if (d->nlayers > 1) return SSM_ERR_UNSUPPORTED;  // one layer per prefill
     if (pool == nullptr) return SSM_ERR_NULL;
     if (pool->reserved != 0 || ws_bytes < 0) return SSM_ERR_SHAPE;
     if (d->batch == 0) return SSM_OK;
@@ -1939,7 +1949,7 @@ int ssm_step_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x,
 }
 
 int64_t ssm_prefill_workspace_bytes(const ssm_desc_t *desc) {
-    if (check_desc(desc) != SSM_OK || desc->batch == 0) return 0;
+    if (check_desc(desc) != SSM_OK || desc->batch == 0 || desc->nlayers > 1) return 0;
     const int L = prefill_chunk_len(desc, -1);
     return L == 0 ? 0 : prefill_ws_bytes(desc, L);
 }
@@ -1954,6 +1964,7 @@ int ssm_prefill_scratch(const ssm_desc_t *desc, const ssm_pool_t *pool, const vo
                         const void *dt, const float *A, const float *D, float *y, uint32_t *dev_status, void *stream) {
     const int rc = check_desc(desc);
     if (rc != SSM_OK) return rc;
+    if (desc->nlayers > 1) return SSM_ERR_UNSUPPORTED;
     if (pool == nullptr) return SSM_ERR_NULL;
     if (desc->batch == 0) return SSM_OK;
     const int64_t need = ssm_prefill_workspace_bytes(desc);

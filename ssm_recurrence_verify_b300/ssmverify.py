@@ -46,7 +46,7 @@ EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify",
 class SsmDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
                 ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("ntok", ctypes.c_int32),
-                ("in_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("in_dtype", ctypes.c_int32), ("nlayers", ctypes.c_int32)]
 
 
 class PoolDesc(ctypes.Structure):
@@ -149,7 +149,9 @@ def make_desc(state_shape, x_shape, B_shape, in_dtype: int) -> SsmDesc:
 
 def _validate(state, x, B, C, dt, A, D, accept_len, y, pooled=False):
     """Check the tensors of one call; with `pooled`, `state` is a pool
-    [nslots][H][P][N] and the batch comes from x."""
+    [nslots][H][P][N] and the batch comes from x. A 5-D state
+    [L][batch][H][P][N] makes the call a layer stack: x, B, C, dt, y then
+    carry the same leading [L], A and D are [L][H], accept_len stays [batch]."""
     tensors = {"state": state, "x": x, "B": B, "dt": dt, "A": A}
     for k, v in (("C", C), ("D", D), ("accept_len", accept_len), ("y", y)):
         if v is not None:
@@ -160,36 +162,38 @@ def _validate(state, x, B, C, dt, A, D, accept_len, y, pooled=False):
             raise ValueError(f"{k} must be a CUDA tensor on {dev}")
         if not v.is_contiguous():
             raise ValueError(f"{k} must be contiguous")
-    if state.dtype != torch.float32 or state.dim() != 4:
-        raise ValueError("state must be float32 [batch][H][P][N]")
-    _, H, P, N = state.shape
-    bsz = x.shape[0] if pooled else state.shape[0]
-    if x.dim() != 4 or x.shape[0] != bsz or x.shape[2] != H or x.shape[3] != P:
-        raise ValueError(f"x must be [batch][K][H][P] = [{bsz}][K][{H}][{P}], got {tuple(x.shape)}")
-    K = x.shape[1]
-    if B.dim() != 4 or B.shape[0] != bsz or B.shape[1] != K or B.shape[3] != N:
-        raise ValueError(f"B must be [batch][K][G][N], got {tuple(B.shape)}")
-    G = B.shape[2]
+    if state.dtype != torch.float32 or state.dim() not in ((4,) if pooled else (4, 5)):
+        raise ValueError("state must be float32 [batch][H][P][N]" + ("" if pooled else " or [L][batch][H][P][N]"))
+    lead = tuple(state.shape[:-4])  # (L,) for a layer stack
+    H, P, N = state.shape[-3:]
+    bsz = x.shape[len(lead)] if pooled else state.shape[-4]
+    nd = len(lead) + 4
+    if x.dim() != nd or tuple(x.shape[:len(lead)]) != lead or x.shape[-4] != bsz or tuple(x.shape[-2:]) != (H, P):
+        raise ValueError(f"x must be {list(lead)}[batch][K][H][P] = {list(lead)}[{bsz}][K][{H}][{P}], "
+                         f"got {tuple(x.shape)}")
+    K = x.shape[-3]
+    if B.dim() != nd or tuple(B.shape[:len(lead)]) != lead or tuple(B.shape[-4:-2]) != (bsz, K) or B.shape[-1] != N:
+        raise ValueError(f"B must be {list(lead)}[batch][K][G][N], got {tuple(B.shape)}")
+    G = B.shape[-2]
     if C is not None and tuple(C.shape) != tuple(B.shape):
         raise ValueError("C must have B's shape")
-    if tuple(dt.shape) != (bsz, K, H):
-        raise ValueError(f"dt must be [batch][K][H] = [{bsz}][{K}][{H}], got {tuple(dt.shape)}")
+    if tuple(dt.shape) != lead + (bsz, K, H):
+        raise ValueError(f"dt must be {list(lead)}[batch][K][H] = {list(lead + (bsz, K, H))}, got {tuple(dt.shape)}")
     dts = {x.dtype, B.dtype, dt.dtype} | ({C.dtype} if C is not None else set())
     if len(dts) != 1:
         raise ValueError("x, B, C, dt must share one dtype")
     for k, v in (("A", A), ("D", D)):
-        if v is not None and (v.dtype != torch.float32 or tuple(v.shape) != (H,)):
-            raise ValueError(f"{k} must be float32 [H]")
+        if v is not None and (v.dtype != torch.float32 or tuple(v.shape) != lead + (H,)):
+            raise ValueError(f"{k} must be float32 {list(lead)}[H]")
     if accept_len is not None and (accept_len.dtype != torch.int32 or tuple(accept_len.shape) != (bsz,)):
         raise ValueError("accept_len must be int32 [batch]")
-    if y is not None and (y.dtype != torch.float32 or tuple(y.shape) != (bsz, K, H, P)):
-        raise ValueError("y must be float32 [batch][K][H][P]")
-    return SsmDesc(bsz, H, P, N, G, K, _in_dtype(x), 0), G
+    if y is not None and (y.dtype != torch.float32 or tuple(y.shape) != tuple(x.shape)):
+        raise ValueError(f"y must be float32 {list(lead)}[batch][K][H][P]")
+    return SsmDesc(bsz, H, P, N, G, K, _in_dtype(x), lead[0] if lead else 0), G
 
 
 def _new_y(state, x):
-    bsz, K, H, P = x.shape
-    return torch.empty((bsz, K, H, P), dtype=torch.float32, device=state.device)
+    return torch.empty(tuple(x.shape), dtype=torch.float32, device=state.device)
 
 
 def verify(state, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
@@ -225,11 +229,13 @@ def commit_verify(state, x_prev, B_prev, dt_prev, accept_len_prev, x, B, C, dt, 
     it: y for every new token. Equals commit(...) then verify(...)."""
     y = _new_y(state, x) if y is None else y
     desc, G = _validate(state, x, B, C, dt, A, D, None, y)
-    bsz, H, P, N = state.shape
-    if x_prev.dim() != 4 or x_prev.shape[0] != bsz or x_prev.shape[2:] != (H, P):
-        raise ValueError(f"x_prev must be [batch][K_prev][H][P], got {tuple(x_prev.shape)}")
-    kp = x_prev.shape[1]
-    for k, v, shape in (("B_prev", B_prev, (bsz, kp, G, N)), ("dt_prev", dt_prev, (bsz, kp, H))):
+    lead = tuple(state.shape[:-4])
+    bsz, H, P, N = state.shape[-4:]
+    if (x_prev.dim() != len(lead) + 4 or tuple(x_prev.shape[:len(lead)]) != lead or x_prev.shape[-4] != bsz
+            or tuple(x_prev.shape[-2:]) != (H, P)):
+        raise ValueError(f"x_prev must be {list(lead)}[batch][K_prev][H][P], got {tuple(x_prev.shape)}")
+    kp = x_prev.shape[-3]
+    for k, v, shape in (("B_prev", B_prev, lead + (bsz, kp, G, N)), ("dt_prev", dt_prev, lead + (bsz, kp, H))):
         if tuple(v.shape) != shape:
             raise ValueError(f"{k} must be {list(shape)}, got {tuple(v.shape)}")
     for k, v in (("x_prev", x_prev), ("B_prev", B_prev), ("dt_prev", dt_prev)):

@@ -82,7 +82,7 @@ BASE = 1 << 40  # fake, never dereferenced: every call below fails validation
 
 
 def desc(**kw):
-    d = dict(batch=2, nheads=4, headdim=32, dstate=128, ngroups=2, ntok=3, in_dtype=sv.SSM_BF16, reserved=0)
+    d = dict(batch=2, nheads=4, headdim=32, dstate=128, ngroups=2, ntok=3, in_dtype=sv.SSM_BF16, nlayers=0)
     d.update(kw)
     return sv.SsmDesc(**d)
 
@@ -120,7 +120,7 @@ def test_null_desc_and_pointers(lib):
 @pytest.mark.parametrize("field,value,code", [
     ("batch", -1, sv.SSM_ERR_SHAPE), ("nheads", 0, sv.SSM_ERR_SHAPE), ("headdim", 0, sv.SSM_ERR_SHAPE),
     ("ngroups", 3, sv.SSM_ERR_SHAPE), ("ngroups", 0, sv.SSM_ERR_SHAPE), ("ntok", 0, sv.SSM_ERR_SHAPE),
-    ("reserved", 1, sv.SSM_ERR_SHAPE), ("dstate", 96, sv.SSM_ERR_UNSUPPORTED), ("dstate", 512, sv.SSM_ERR_UNSUPPORTED),
+    ("nlayers", -1, sv.SSM_ERR_SHAPE), ("dstate", 96, sv.SSM_ERR_UNSUPPORTED), ("dstate", 512, sv.SSM_ERR_UNSUPPORTED),
     ("dstate", 8, sv.SSM_ERR_UNSUPPORTED), ("in_dtype", 7, sv.SSM_ERR_UNSUPPORTED),
 ])
 def test_shape_errors(lib, field, value, code):
@@ -326,6 +326,27 @@ def test_binding_arities_match_header(lib):
         argtypes = getattr(lib, name).argtypes
         if argtypes is not None:
             assert len(argtypes) == _arity(name), name
+
+
+@no_gpu_only
+def test_layer_stack_validation(lib):
+    """nlayers = L scales every per-layer buffer by L (accept_len stays [batch]);
+    pool entry points and prefill take one layer."""
+    xb = 2 * 3 * 4 * 32 * 2  # bytes of one layer's x: batch 2, K 3, H 4, P 32, bf16
+    for L, code in ((0, sv.SSM_ERR_CUDA), (1, sv.SSM_ERR_CUDA), (3, sv.SSM_ERR_ALIAS)):
+        p = ptrs(10)
+        p[8] = ctypes.c_void_p(p[1].value + xb + 64)  # y just past layer 0's x: inside layer 1's
+        assert vc(lib, desc(nlayers=L), p) == code, L
+    p = ptrs(10)
+    assert vc(lib, desc(nlayers=64), p) == sv.SSM_ERR_CUDA  # valid: the launch fails on this host
+    st = ptrs(1)[0].value
+    args = ptrs(9, start=BASE + (1 << 35))
+    assert lib.ssm_verify_commit_pool(ctypes.byref(desc(nlayers=2)), ctypes.byref(pool(st)), *args,
+                                      None) == sv.SSM_ERR_UNSUPPORTED
+    pargs = ptrs(7, start=BASE + (1 << 35))
+    assert lib.ssm_prefill(ctypes.byref(desc(nlayers=2)), ctypes.byref(pool(st)), *pargs, None, 0, None,
+                           None) == sv.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_prefill_workspace_bytes(ctypes.byref(desc(nlayers=2, batch=1, ntok=2048))) == 0
 
 
 def pool(states, slot=None, nslots=4, reserved=0):

@@ -250,3 +250,90 @@ def test_long_decode_slow_decay(cuda_device, K, dtype):
     y = torch.cat(ys, dim=1)
     torch.cuda.synchronize()
     _check(y, st, ref, wl.torch_in_dtype, f"long decode K={K}")
+
+
+def _stack(ds, keys):
+    return {k: torch.stack([d[k] for d in ds]) for k in keys}
+
+
+@pytest.mark.parametrize("K,dtype", [(8, synth.BF16), (12, synth.F32)])
+def test_layer_stack_equals_per_layer_calls(cuda_device, K, dtype):
+    """nlayers = L: one call over [L]-leading slabs (A, D [L][H]; accept_len
+    [batch] shared) gives, bit for bit, the L single-layer calls on the
+    slices, in every entry point."""
+    dev = cuda_device
+    L, batch = 3, 5
+    wl = synth.custom_workload(batch, 4, 64, 128, 2, K, dtype, seed=880 + K)
+    ds = [synth.draw_layer_round(wl, rnd=0, layer=l) for l in range(L)]
+    acc = ds[0]["accept_len"].to(dev)
+    S = {k: v.to(dev) for k, v in _stack(ds, ("state0", "x", "B", "C", "dt", "A", "D")).items()}
+    nxt = [synth.draw_tokens(wl, 1, l) for l in range(L)]
+    N2 = {k: v.to(dev) for k, v in _stack(nxt, ("x", "B", "C", "dt")).items()}
+
+    # verify
+    y = ssm.verify(S["state0"], S["x"], S["B"], S["C"], S["dt"], S["A"], S["D"])
+    for l in range(L):
+        yl = ssm.verify(S["state0"][l], S["x"][l], S["B"][l], S["C"][l], S["dt"][l], S["A"][l], S["D"][l])
+        assert torch.equal(y[l], yl), ("verify", l)
+    # verify_commit, commit, step, commit_verify: state in place
+    for fn in ("verify_commit", "commit", "step", "commit_verify"):
+        st = S["state0"].clone()
+        per = S["state0"].clone()
+        if fn == "verify_commit":
+            y = ssm.verify_commit(st, S["x"], S["B"], S["C"], S["dt"], S["A"], S["D"], acc)
+            ys = [ssm.verify_commit(per[l], S["x"][l], S["B"][l], S["C"][l], S["dt"][l], S["A"][l], S["D"][l], acc)
+                  for l in range(L)]
+        elif fn == "commit":
+            ssm.commit(st, S["x"], S["B"], S["dt"], S["A"], acc)
+            for l in range(L):
+                ssm.commit(per[l], S["x"][l], S["B"][l], S["dt"][l], S["A"][l], acc)
+            y, ys = None, None
+        elif fn == "step":
+            one = {k: S[k][:, :, :1].contiguous() for k in ("x", "B", "C", "dt")}
+            y = ssm.step(st, one["x"], one["B"], one["C"], one["dt"], S["A"], S["D"])
+            ys = [ssm.step(per[l], one["x"][l], one["B"][l], one["C"][l], one["dt"][l], S["A"][l], S["D"][l])
+                  for l in range(L)]
+        else:
+            y = ssm.commit_verify(st, S["x"], S["B"], S["dt"], acc, N2["x"], N2["B"], N2["C"], N2["dt"], S["A"],
+                                  S["D"])
+            ys = [ssm.commit_verify(per[l], S["x"][l], S["B"][l], S["dt"][l], acc, N2["x"][l], N2["B"][l],
+                                    N2["C"][l], N2["dt"][l], S["A"][l], S["D"][l]) for l in range(L)]
+        torch.cuda.synchronize()
+        assert torch.equal(st, per), fn
+        if y is not None:
+            for l in range(L):
+                assert torch.equal(y[l], ys[l]), (fn, l)
+    # against the oracle, layer by layer
+    st = S["state0"].clone()
+    y = ssm.verify_commit(st, S["x"], S["B"], S["C"], S["dt"], S["A"], S["D"], acc)
+    torch.cuda.synchronize()
+    for l in range(L):
+        d = ds[l]
+        ref = oracle.verify_commit(d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], d["accept_len"])
+        _check(y[l], st[l], ref, wl.torch_in_dtype, f"stack layer {l}")
+
+
+def test_hybrid_16_layer_stack_rounds(cuda_device):
+    """The 16-layer hybrid workload as one stacked verify_commit per round
+    (every layer shares the round's accept_len), state carried across
+    rounds, each layer against the oracle."""
+    dev = cuda_device
+    wl = synth.WORKLOADS[2]
+    L = wl.nlayers
+    ps = [synth.draw_params(wl, l) for l in range(L)]
+    P_ = {k: torch.stack([p[k] for p in ps]).to(dev) for k in ("state0", "A", "D")}
+    st = P_["state0"].clone()
+    s64 = [p["state0"].double().numpy() for p in ps]
+    for rnd in range(wl.rounds):
+        ts = [synth.draw_tokens(wl, rnd, l) for l in range(L)]
+        T_ = {k: torch.stack([t[k] for t in ts]).to(dev) for k in ("x", "B", "C", "dt")}
+        acc = synth.draw_accept_len(wl, rnd)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        y = ssm.verify_commit(st, T_["x"], T_["B"], T_["C"], T_["dt"], P_["A"], P_["D"], acc.to(dev),
+                              dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for l in range(L):
+            ref = _oracle_round(s64[l], ts[l], ps[l], acc)
+            _check(y[l], st[l], ref, wl.torch_in_dtype, f"{wl.name} layer {l} round {rnd}")
+            s64[l] = ref["state"]
