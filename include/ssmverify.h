@@ -110,7 +110,8 @@ typedef struct {
 
 /*
  * Layer stacks (desc->nlayers = L > 1; ssm_verify, ssm_commit,
- * ssm_verify_commit, ssm_commit_verify and ssm_step). A hybrid model runs the
+ * ssm_verify_commit, ssm_commit_verify, ssm_step and their pool variants).
+ * A hybrid model runs the
  * same K draft tokens through every Mamba layer, each layer with its own
  * cached state and its own inputs (the speculative-decoding section: every
  * Mamba layer of the verifier rolls back to the same last accepted token).
@@ -119,9 +120,11 @@ typedef struct {
  * above (state [L][batch][nheads][headdim][dstate], x [L][batch][ntok]
  * [nheads][headdim], ...), A and D are [L][nheads], and accept_len (and
  * accept_len_prev) stays [batch]: one accepted prefix per sequence, shared
- * by every layer. The result equals L single-layer calls on the slices; the
- * pool entry points and prefill take one layer (L > 1 there:
- * SSM_ERR_UNSUPPORTED). nlayers < 0: SSM_ERR_SHAPE.
+ * by every layer. A pool is then [L][nslots][nheads][headdim][dstate] (layer
+ * l's pool is states[l]) and slot[batch] maps a sequence to the same slot in
+ * every layer. The result equals L single-layer calls on the slices. Prefill
+ * takes one layer (L > 1 there: SSM_ERR_UNSUPPORTED). nlayers < 0:
+ * SSM_ERR_SHAPE.
  */
 
 /*
@@ -208,7 +211,7 @@ int ssm_step(const ssm_desc_t *desc, float *state, const void *x, const void *B,
  * ------------------------------------------------------------------------ */
 
 typedef struct {
-    float *states;        /* [nslots][nheads][headdim][dstate] fp32, 16-byte aligned */
+    float *states;        /* [nslots][nheads][headdim][dstate] fp32 ([nlayers][nslots]... for a layer stack), 16-byte aligned */
     const int32_t *slot;  /* [batch] slot of each sequence, device memory; NULL: sequence b uses slot b */
     int32_t nslots;       /* >= 1; >= batch when slot is NULL */
     int32_t reserved;     /* must be 0 */

@@ -388,10 +388,14 @@ __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, in
     T.rows = min(kRows, a.P - T.row0);
     long long sb = T.b;
     T.ok = true;
-    if (POOL && a.slot != nullptr) {
-        const int s = __ldg(a.slot + T.b);
-        T.ok = s >= 0 && s < a.nslots;
-        sb = T.ok ? s : 0;  // an invalid slot reads slot 0 (in bounds) and writes nothing
+    if (POOL) {  // layer l's pool is states[l]: [nslots] sequence states
+        int s = T.bs;
+        if (a.slot != nullptr) {
+            s = __ldg(a.slot + T.bs);
+            T.ok = s >= 0 && s < a.nslots;
+            if (!T.ok) s = 0;  // an invalid slot reads slot 0 (in bounds) and writes nothing
+        }
+        sb = (long long)T.lay * a.nslots + s;
     }
     T.sbase = (sb * a.H + T.h) * (long long)a.P * N;
     return T;
@@ -1463,7 +1467,6 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     const int N = d->dstate;
     const int ROWS = rows_per_tile(N);
     const int64_t nl = d->nlayers > 1 ? d->nlayers : 1;  // layers; a stack is nl x batch sequences
-    if (nl > 1 && c.pool) return SSM_ERR_UNSUPPORTED;
     const int64_t ptiles = (d->headdim + ROWS - 1) / ROWS;
     const int64_t ntiles = nl * d->batch * d->nheads * ptiles;
     if (ntiles >= (int64_t)1 << 31) return SSM_ERR_SHAPE;
@@ -1493,10 +1496,10 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
 
     // B_: sequences of the call (all layers); accept_len covers one layer's d->batch
     const int64_t B_ = nl * d->batch, H = d->nheads, P = d->headdim, G = d->ngroups;
-    const int64_t state_bytes = (c.pool ? (int64_t)c.nslots : B_) * H * P * N * 4;
+    const int64_t state_bytes = (c.pool ? nl * c.nslots : B_) * H * P * N * 4;
     BufList bl;
     if (st != nullptr) bl.add(st, state_bytes, F != kVerify);
-    if (c.pool && c.slot != nullptr) bl.add(c.slot, B_ * 4, false);
+    if (c.pool && c.slot != nullptr) bl.add(c.slot, (int64_t)d->batch * 4, false);
     bl.add(c.A, nl * H * 4, false);
     if (verify_phase) {
         const int64_t bk = B_ * d->ntok;

@@ -162,8 +162,9 @@ def _validate(state, x, B, C, dt, A, D, accept_len, y, pooled=False):
             raise ValueError(f"{k} must be a CUDA tensor on {dev}")
         if not v.is_contiguous():
             raise ValueError(f"{k} must be contiguous")
-    if state.dtype != torch.float32 or state.dim() not in ((4,) if pooled else (4, 5)):
-        raise ValueError("state must be float32 [batch][H][P][N]" + ("" if pooled else " or [L][batch][H][P][N]"))
+    if state.dtype != torch.float32 or state.dim() not in (4, 5):
+        raise ValueError("state must be float32 [batch][H][P][N] or [L][batch][H][P][N]"
+                         + (" (a pool: [nslots] or [L][nslots] in place of batch)" if pooled else ""))
     lead = tuple(state.shape[:-4])  # (L,) for a layer stack
     H, P, N = state.shape[-3:]
     bsz = x.shape[len(lead)] if pooled else state.shape[-4]
@@ -340,22 +341,25 @@ def accept_sample(target_logits, draft_logits, draft_tokens, uniform, accept_len
 # ----------------------------------------------------------------------------- state pool and prefill
 
 def _pool(states: torch.Tensor, slot: Optional[torch.Tensor], bsz: int):
-    """The C pool descriptor: `states` [nslots][H][P][N] fp32 CUDA, `slot`
-    int32 [batch] CUDA (None: sequence b uses slot b)."""
-    if not states.is_cuda or states.dtype != torch.float32 or states.dim() != 4 or not states.is_contiguous():
-        raise ValueError("pool states must be a contiguous float32 CUDA tensor [nslots][H][P][N]")
+    """The C pool descriptor: `states` [nslots][H][P][N] fp32 CUDA (a layer
+    stack: [L][nslots][H][P][N]), `slot` int32 [batch] CUDA (None: sequence b
+    uses slot b), the same slot in every layer."""
+    if not states.is_cuda or states.dtype != torch.float32 or states.dim() not in (4, 5) or \
+            not states.is_contiguous():
+        raise ValueError("pool states must be a contiguous float32 CUDA tensor [nslots][H][P][N] "
+                         "or [L][nslots][H][P][N]")
     if slot is not None:
         if not slot.is_cuda or slot.device != states.device or slot.dtype != torch.int32 or \
                 tuple(slot.shape) != (bsz,) or not slot.is_contiguous():
             raise ValueError(f"slot must be a contiguous int32 CUDA tensor [{bsz}] on {states.device}")
-    return PoolDesc(states.data_ptr(), None if slot is None else slot.data_ptr(), states.shape[0], 0)
+    return PoolDesc(states.data_ptr(), None if slot is None else slot.data_ptr(), states.shape[-4], 0)
 
 
 def verify_pool(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
     """verify on the pool slots `slot` of `states` (read only)."""
     y = _new_y(states, x) if y is None else y
     desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
-    pool = _pool(states, slot, x.shape[0])
+    pool = _pool(states, slot, desc.batch)
     _check(load_library().ssm_verify_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
                                           _ptr(dt), _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
@@ -364,7 +368,7 @@ def verify_pool(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream
 def commit_pool(states, slot, x, B, dt, A, accept_len, dev_status=None, stream=None) -> None:
     """commit into the pool slots."""
     desc, _ = _validate(states, x, B, None, dt, A, None, accept_len, None, pooled=True)
-    pool = _pool(states, slot, x.shape[0])
+    pool = _pool(states, slot, desc.batch)
     _check(load_library().ssm_commit_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(dt),
                                           _ptr(A), _ptr(accept_len), _ptr(dev_status), _stream(stream)))
 
@@ -374,7 +378,7 @@ def verify_commit_pool(states, slot, x, B, C, dt, A, D, accept_len, y=None, dev_
     """verify_commit on the pool slots."""
     y = _new_y(states, x) if y is None else y
     desc, _ = _validate(states, x, B, C, dt, A, D, accept_len, y, pooled=True)
-    pool = _pool(states, slot, x.shape[0])
+    pool = _pool(states, slot, desc.batch)
     _check(load_library().ssm_verify_commit_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
                                                  _ptr(dt), _ptr(A), _ptr(D), _ptr(accept_len), _ptr(y),
                                                  _ptr(dev_status), _stream(stream)))
@@ -386,11 +390,12 @@ def commit_verify_pool(states, slot, x_prev, B_prev, dt_prev, accept_len_prev, x
     """commit_verify on the pool slots."""
     y = _new_y(states, x) if y is None else y
     desc, G = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
-    bsz = x.shape[0]
-    _, H, P, N = states.shape
-    kp = x_prev.shape[1]
-    for k, v, shape in (("x_prev", x_prev, (bsz, kp, H, P)), ("B_prev", B_prev, (bsz, kp, G, N)),
-                        ("dt_prev", dt_prev, (bsz, kp, H))):
+    bsz = desc.batch
+    lead = tuple(states.shape[:-4])
+    H, P, N = states.shape[-3:]
+    kp = x_prev.shape[-3] if x_prev.dim() >= 3 else 0
+    for k, v, shape in (("x_prev", x_prev, lead + (bsz, kp, H, P)), ("B_prev", B_prev, lead + (bsz, kp, G, N)),
+                        ("dt_prev", dt_prev, lead + (bsz, kp, H))):
         if tuple(v.shape) != shape or v.dtype != x.dtype or not v.is_cuda or not v.is_contiguous():
             raise ValueError(f"{k} must be a contiguous {x.dtype} CUDA tensor {list(shape)}")
     if accept_len_prev.dtype != torch.int32 or tuple(accept_len_prev.shape) != (bsz,) or not accept_len_prev.is_cuda:
@@ -407,7 +412,7 @@ def step_pool(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream=N
     """step (K = 1) on the pool slots."""
     y = _new_y(states, x) if y is None else y
     desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
-    pool = _pool(states, slot, x.shape[0])
+    pool = _pool(states, slot, desc.batch)
     _check(load_library().ssm_step_pool(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
                                         _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y
@@ -427,7 +432,7 @@ def prefill(states, slot, x, B, C, dt, A, D, y=None, workspace=None, dev_status=
     by default it is allocated here at the size the library asks for."""
     y = _new_y(states, x) if y is None else y
     desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
-    pool = _pool(states, slot, x.shape[0])
+    pool = _pool(states, slot, desc.batch)
     lib = load_library()
     if workspace is None:
         nbytes = int(lib.ssm_prefill_workspace_bytes(ctypes.byref(desc)))
@@ -446,7 +451,7 @@ def prefill_scratch(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, st
     whose workspace exceeds SSM_PREFILL_SCRATCH_BYTES are rejected."""
     y = _new_y(states, x) if y is None else y
     desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
-    pool = _pool(states, slot, x.shape[0])
+    pool = _pool(states, slot, desc.batch)
     _check(load_library().ssm_prefill_scratch(ctypes.byref(desc), ctypes.byref(pool), _ptr(x), _ptr(B), _ptr(C),
                                               _ptr(dt), _ptr(A), _ptr(D), _ptr(y), _ptr(dev_status), _stream(stream)))
     return y

@@ -330,8 +330,8 @@ def test_binding_arities_match_header(lib):
 
 @no_gpu_only
 def test_layer_stack_validation(lib):
-    """nlayers = L scales every per-layer buffer by L (accept_len stays [batch]);
-    pool entry points and prefill take one layer."""
+    """nlayers = L scales every per-layer buffer (and a pool) by L; accept_len
+    and the slot map stay [batch]; prefill takes one layer."""
     xb = 2 * 3 * 4 * 32 * 2  # bytes of one layer's x: batch 2, K 3, H 4, P 32, bf16
     for L, code in ((0, sv.SSM_ERR_CUDA), (1, sv.SSM_ERR_CUDA), (3, sv.SSM_ERR_ALIAS)):
         p = ptrs(10)
@@ -341,8 +341,17 @@ def test_layer_stack_validation(lib):
     assert vc(lib, desc(nlayers=64), p) == sv.SSM_ERR_CUDA  # valid: the launch fails on this host
     st = ptrs(1)[0].value
     args = ptrs(9, start=BASE + (1 << 35))
+    # a stacked pool is [L][nslots][H][P][N]: valid (the launch fails on this host) ...
     assert lib.ssm_verify_commit_pool(ctypes.byref(desc(nlayers=2)), ctypes.byref(pool(st)), *args,
-                                      None) == sv.SSM_ERR_UNSUPPORTED
+                                      None) == sv.SSM_ERR_CUDA
+    # ... and y just past layer 0's pool lies inside layer 1's
+    pb = 4 * 4 * 32 * 128 * 4  # nslots 4 x H 4 x P 32 x N 128 x fp32
+    a2 = list(args)
+    a2[7] = ctypes.c_void_p(st + pb + 64)
+    assert lib.ssm_verify_commit_pool(ctypes.byref(desc(nlayers=1)), ctypes.byref(pool(st)), *a2,
+                                      None) == sv.SSM_ERR_CUDA
+    assert lib.ssm_verify_commit_pool(ctypes.byref(desc(nlayers=2)), ctypes.byref(pool(st)), *a2,
+                                      None) == sv.SSM_ERR_ALIAS
     pargs = ptrs(7, start=BASE + (1 << 35))
     assert lib.ssm_prefill(ctypes.byref(desc(nlayers=2)), ctypes.byref(pool(st)), *pargs, None, 0, None,
                            None) == sv.SSM_ERR_UNSUPPORTED

@@ -203,3 +203,57 @@ def test_prefill_then_speculative_round(cuda_device):
     r1 = oracle.verify_commit(zero, t["x"], t["B"], t["C"], t["dt"], p["A"], p["D"], None)
     r2 = oracle.verify_commit(r1["state"], t2["x"], t2["B"], t2["C"], t2["dt"], p["A"], p["D"], acc)
     assert rel_err(np64(y), r2["y"]) <= 1e-4 and rel_err(np64(pool), r2["state"]) <= 1e-4
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_pool_layer_stack_equals_per_layer_pool_calls(cuda_device, dtype):
+    """A stacked pool [L][nslots][H][P][N] with one slot map for every layer:
+    each pool entry point over the stack equals, bit for bit, the per-layer
+    pool calls on states[l]; a bad slot writes nothing in any layer."""
+    dev = cuda_device
+    L, batch, nslots, K = 3, 4, 7, 8
+    wl = synth.custom_workload(batch, 4, 64, 128, 2, K, dtype, seed=990)
+    ds = [synth.draw_layer_round(wl, rnd=0, layer=l) for l in range(L)]
+    S = {k: torch.stack([d[k] for d in ds]).to(dev) for k in ("x", "B", "C", "dt", "A", "D")}
+    acc = ds[0]["accept_len"].to(dev)
+    g = torch.Generator().manual_seed(5)
+    pool0 = (0.1 * torch.randn(L, nslots, 4, 64, 128, generator=g)).to(dev)
+    slot = torch.tensor([5, 0, 9, 2], dtype=torch.int32, device=dev)  # slot 9: out of range
+    nxt = [synth.draw_tokens(wl, 1, l) for l in range(L)]
+    N2 = {k: torch.stack([t[k] for t in nxt]).to(dev) for k in ("x", "B", "C", "dt")}
+    one = {k: S[k][:, :, :1].contiguous() for k in ("x", "B", "C", "dt")}
+
+    def run(fn, pool, l=None):
+        sel = (lambda t: t) if l is None else (lambda t: t[l])
+        st = pool if l is None else pool[l]
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if fn == "verify":
+            y = ssm.verify_pool(st, slot, *(sel(S[k]) for k in ("x", "B", "C", "dt", "A", "D")), dev_status=status)
+        elif fn == "verify_commit":
+            y = ssm.verify_commit_pool(st, slot, *(sel(S[k]) for k in ("x", "B", "C", "dt", "A", "D")), acc,
+                                       dev_status=status)
+        elif fn == "commit":
+            ssm.commit_pool(st, slot, sel(S["x"]), sel(S["B"]), sel(S["dt"]), sel(S["A"]), acc, dev_status=status)
+            y = None
+        elif fn == "commit_verify":
+            y = ssm.commit_verify_pool(st, slot, sel(S["x"]), sel(S["B"]), sel(S["dt"]), acc,
+                                       *(sel(N2[k]) for k in ("x", "B", "C", "dt")), sel(S["A"]), sel(S["D"]),
+                                       dev_status=status)
+        else:
+            y = ssm.step_pool(st, slot, *(sel(one[k]) for k in ("x", "B", "C", "dt")), sel(S["A"]), sel(S["D"]),
+                              dev_status=status)
+        return y, status
+
+    for fn in ("verify", "verify_commit", "commit", "commit_verify", "step"):
+        stacked = pool0.clone()
+        per = pool0.clone()
+        y, status = run(fn, stacked)
+        outs = [run(fn, per, l) for l in range(L)]
+        torch.cuda.synchronize()
+        assert torch.equal(stacked, per), fn
+        assert int(status.item()) & ssm.ssmverify.SSM_STATUS_BAD_SLOT, fn
+        if y is not None:
+            for l in range(L):
+                assert torch.equal(y[l][torch.tensor([0, 1, 3])], outs[l][0][torch.tensor([0, 1, 3])]), (fn, l)
+        untouched = [i for i in range(nslots) if i not in (5, 0, 2)]
+        assert torch.equal(stacked[:, untouched], pool0[:, untouched]), fn
