@@ -83,3 +83,58 @@ def test_prefill_then_speculative_rounds(cuda_device, rule):
     untouched = [i for i in range(6) if i not in slot.tolist()]
     assert (pool[untouched] == 0).all()
     assert len({int(a) for a_ in accs for a in a_.cpu()}) > 1  # the rounds accept different prefixes
+
+
+def test_layer_stack_serving_loop(cuda_device):
+    """The serving loop of a hybrid model with L Mamba layers: each layer's
+    prompt prefilled into its pool states[l]; then every round one stacked
+    commit_verify_pool call over all layers (accept_len from the device's
+    greedy acceptance of the previous round, shared by the layers); a last
+    stacked commit. Every layer against the oracle chain."""
+    dev = cuda_device
+    L, batch, H, P, N, G, K, T, V, rounds = 3, 3, 4, 64, 128, 2, 4, 40, 300, 3
+    prompt = synth.custom_workload(batch, H, P, N, G, T, synth.BF16, seed=711)
+    draft = synth.custom_workload(batch, H, P, N, G, K, synth.BF16, seed=712)
+    ps = [synth.draw_params(prompt, l) for l in range(L)]
+    A = torch.stack([p["A"] for p in ps]).to(dev)
+    D = torch.stack([p["D"] for p in ps]).to(dev)
+    slot = torch.tensor([2, 4, 0], dtype=torch.int32, device=dev)
+    pool = torch.zeros(L, 5, H, P, N, device=dev)
+
+    tps = [synth.draw_tokens(prompt, 0, l) for l in range(L)]
+    for l in range(L):
+        t = {k: v.to(dev) for k, v in tps[l].items()}
+        ssm.prefill(pool[l], slot, t["x"], t["B"], t["C"], t["dt"], A[l], D[l])
+
+    ys, accs, blocks, prev = [], [], [], None
+    for r in range(rounds):
+        ts = [synth.draw_tokens(draft, r, l) for l in range(L)]
+        td = {k: torch.stack([t[k] for t in ts]).to(dev) for k in ("x", "B", "C", "dt")}
+        if prev is None:
+            y = ssm.verify_pool(pool, slot, td["x"], td["B"], td["C"], td["dt"], A, D)
+        else:
+            y = ssm.commit_verify_pool(pool, slot, prev["x"], prev["B"], prev["dt"], prev["acc"], td["x"], td["B"],
+                                       td["C"], td["dt"], A, D)
+        lg = synth.draw_accept_inputs(synth.custom_accept_workload(batch, K, V, synth.F32, seed=820 + r))
+        a_len, _ = ssm.accept_greedy(lg["target_logits"].to(dev), lg["draft_tokens"].to(dev))
+        ys.append(y)
+        accs.append(a_len)
+        blocks.append(ts)
+        prev = {"x": td["x"], "B": td["B"], "dt": td["dt"], "acc": a_len}
+    ssm.commit_pool(pool, slot, prev["x"], prev["B"], prev["dt"], A, prev["acc"])
+    torch.cuda.synchronize()
+
+    for l in range(L):
+        tp = tps[l]
+        ref = oracle.verify_commit(np.zeros((batch, H, P, N)), tp["x"], tp["B"], tp["C"], tp["dt"], ps[l]["A"],
+                                   ps[l]["D"], None)
+        state = ref["state"]
+        for r in range(rounds):
+            t = blocks[r][l]
+            out = oracle.verify_commit(state, t["x"], t["B"], t["C"], t["dt"], ps[l]["A"], ps[l]["D"],
+                                       accs[r].cpu())
+            assert rel_err(np64(ys[r][l]), out["y"]) <= y_tol(torch.bfloat16), (l, r)
+            state = out["state"]
+        assert rel_err(np64(pool[l][slot.long()]), state) <= RTOL_STATE, l
+    untouched = [i for i in range(5) if i not in slot.tolist()]
+    assert (pool[:, untouched] == 0).all()
