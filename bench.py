@@ -27,6 +27,7 @@ bounded samples of the same workload, on rank 0 only.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -759,6 +760,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers of a layer stack (a smaller case for profiling)")
     ap.add_argument("--per-layer-launches", action="store_true",
                     help="run a layer stack as one launch per layer instead of one launch over all layers")
     ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill"], default="ssm",
@@ -768,6 +771,10 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = synth.WORKLOADS[args.workload]
+    if args.layers is not None:  # the first `layers` layers of the stack (profiling a smaller case)
+        if not 1 <= args.layers <= wl.nlayers:
+            ap.error(f"--layers must be in [1, {wl.nlayers}]")
+        wl = dataclasses.replace(wl, nlayers=args.layers, name=f"{wl.name}_first{args.layers}layers")
     rank, world, local_rank = dist_env()
 
     if args.impl == "reference":

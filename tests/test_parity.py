@@ -82,6 +82,33 @@ def test_mamba2_stack_sampled_layers(cuda_device):
     run_workload(synth.WORKLOADS[4], cuda_device, layers=[0, 21, 42, 63])
 
 
+def test_mamba2_full_stack_one_launch(cuda_device):
+    """The 64-layer stack as the benchmark launches it: one verify_commit over
+    all 64 layers (2.7 GB of state), every output of layers 0, 21, 42 and 63
+    against the oracle, and the other layers bit for bit against their own
+    single-layer launches on sampled layers 7 and 50."""
+    dev = cuda_device
+    wl = synth.WORKLOADS[4]
+    L = wl.nlayers
+    ds = [synth.draw_layer_round(wl, rnd=0, layer=l) for l in range(L)]
+    acc = ds[0]["accept_len"]
+    S = {k: torch.stack([d[k] for d in ds]).to(dev) for k in ("state0", "x", "B", "C", "dt", "A", "D")}
+    st = S["state0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = ssm.verify_commit(st, S["x"], S["B"], S["C"], S["dt"], S["A"], S["D"], acc.to(dev), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for l in (0, 21, 42, 63):
+        d = ds[l]
+        ref = oracle.verify_commit(d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"], acc)
+        _check(y[l], st[l], ref, wl.torch_in_dtype, f"{wl.name} stacked launch, layer {l}")
+    for l in (7, 50):
+        s1 = S["state0"][l].clone()
+        y1 = ssm.verify_commit(s1, S["x"][l], S["B"][l], S["C"][l], S["dt"][l], S["A"][l], S["D"][l], acc.to(dev))
+        torch.cuda.synchronize()
+        assert torch.equal(s1, st[l]) and torch.equal(y1, y[l]), l
+
+
 SHAPES = [
     # batch, H, P, N, G, K, dtype
     (1, 2, 16, 16, 1, 4, synth.F32),
