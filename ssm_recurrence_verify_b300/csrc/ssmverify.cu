@@ -1129,6 +1129,7 @@ struct CSArgs {
     const void *x, *B, *dt;  // chunk v = tokens v*L .. v*L + L - 1 of the [batch][T] layouts
     const float *A;
     float *ws;               // [chunks][H][P][N]
+    uint32_t *dev_status;    // nullable (the tensor-memory kernel's bounded wait)
     int H, P, G, L, ptiles;
 };
 
@@ -1237,6 +1238,194 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
         *reinterpret_cast<float2 *>(out + (long long)r0 * N + c) = make_float2(acc[nb][0], acc[nb][1]);
         *reinterpret_cast<float2 *>(out + (long long)r1 * N + c) = make_float2(acc[nb][2], acc[nb][3]);
     }
+}
+
+// The same first pass on the 5th-generation tensor cores (tcgen05), for bf16
+// inputs, N = 128, L = 128 and 128-row tiles: one CTA computes
+// S[p][n] = sum_s (w_s u_s[p]) B_s[n] for 128 rows of one head of one chunk
+// as an M = 128, N = 128, K = 128 product accumulated in tensor memory.
+//  * Operands in shared memory, MN-major, no swizzle: 8 (token) x 16-byte
+//    core matrices, row- or state-channel-contiguous as x and B arrive, so
+//    nothing is transposed: element (token s, index i) of an operand sits at
+//    byte (i / 8) * 128 + (s / 8) * 2048 + (s % 8) * 16 + (i % 8) * 2; the
+//    descriptor's leading offset is the token stride (2048), its stride
+//    offset the index stride (128).
+//  * w o U is formed in fp32 by the arithmetic of ssm_chunk_state_kernel and
+//    split into two bf16 parts a1 + a2 (a1 = bf16(a), a2 = bf16(a - a1):
+//    16 significant bits, |a - a1 - a2| <= 2^-18 |a|); B is bf16 and exact.
+//    2 parts x 8 MMAs of K = 16 tokens (tcgen05.mma kind::f16, bf16 x bf16,
+//    fp32 accumulation), issued by one thread; tcgen05.commit signals an
+//    mbarrier, waited on with a time limit. 97 KB of shared memory: two CTAs
+//    per SM, so one CTA's loads overlap the other's products.
+//  * Row p of the accumulator is tensor-memory lane p: warp w reads rows
+//    32w .. 32w + 31 with tcgen05.ld and writes them to the workspace.
+constexpr int kTCRows = 128;
+constexpr int kTCParts = 2;
+struct TCLay {
+    static constexpr int kPart = 128 * 128 * 2;       // one bf16 operand: 128 tokens x 128 indices
+    static constexpr int kA = 0;                      // w o U parts a1, a2
+    static constexpr int kB = kA + kTCParts * kPart;  // B
+    static constexpr int kW = kB + kPart;
+    static constexpr int kW2 = kW + 128 * 4;
+    static constexpr int kDt = kW2 + 128 * 4;
+    static constexpr int kBytes = kDt + 128 * 4;
+};
+
+__device__ __forceinline__ uint32_t tc_operand_off(int s, int i) {
+    return (uint32_t)((i >> 3) * 128 + (s >> 3) * 2048 + (s & 7) * 16 + (i & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: start address, leading byte offset (token
+// direction) 2048, stride byte offset (index direction) 128, version 1, no swizzle.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(2048u >> 4) << 16) | ((uint64_t)(128u >> 4) << 32) |
+           ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// MN-major, N = 128, M = 128.
+constexpr uint32_t kTCIdesc =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t taddr, uint64_t ad, uint64_t bd, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(taddr),
+        "l"(ad), "l"(bd), "r"(kTCIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 v) { return (uint32_t)__bfloat16_as_ushort(v); }
+
+__global__ void __launch_bounds__(128, 2) ssm_chunk_state_tc_kernel(const CSArgs a) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    unsigned char *sbytes = reinterpret_cast<unsigned char *>(ssm_smem);
+    float *sw = sm<float>(TCLay::kW), *sw2 = sm<float>(TCLay::kW2), *sdt = sm<float>(TCLay::kDt);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long t = blockIdx.x;
+    const int ptile = (int)(t % a.ptiles);
+    const long long vh = t / a.ptiles;
+    const int h = (int)(vh % a.H);
+    const long long v = vh / a.H;
+    const int gi = h / (a.H / a.G);
+    const int row0 = ptile * kTCRows;
+    constexpr int L = 128;
+    const float Ah = __ldg(a.A + h);
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(a.x);
+    const __nv_bfloat16 *Bp = static_cast<const __nv_bfloat16 *>(a.B);
+    const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
+
+    // A warp task: 8 consecutive tokens x 4 consecutive 16-byte index chunks, lane (token lane % 8, chunk
+    // lane / 8): a warp's shared stores fill four whole 128-byte lines, and its global reads are 64 bytes
+    // of each of 8 rows. 64 tasks, 16 per warp.
+    auto task_s = [&](int it) { return ((warp + 4 * it) & 15) * 8 + (lane & 7); };
+    auto task_q = [&](int it) { return ((warp + 4 * it) >> 4) * 4 + (lane >> 3); };
+    // B straight into its operand layout, 16 bytes at a time
+#pragma unroll 4
+    for (int it = 0; it < 16; ++it) {
+        const int s = task_s(it), q = task_q(it);
+        cp_async16(sbytes + TCLay::kB + tc_operand_off(s, q * 8), Bp + ((v * L + s) * a.G + gi) * 128LL + q * 8);
+    }
+    // this thread's x vectors, loaded ahead of the product tree
+    uint4 xr[16];
+#pragma unroll
+    for (int it = 0; it < 16; ++it)
+        xr[it] = __ldg(reinterpret_cast<const uint4 *>(x + ((v * L + task_s(it)) * a.H + h) * (long long)a.P + row0 +
+                                                       task_q(it) * 8));
+    // dt and the suffix products w_s = prod_{r > s} Abar_r (the product tree of ssm_chunk_state_kernel)
+    {
+        const float d = ld1(dtp + (v * L + tid) * a.H + h);
+        sdt[tid] = d;
+        sw[tid] = tid + 1 < L ? ssm_decay(ld1(dtp + (v * L + tid + 1) * a.H + h), Ah) : 1.f;
+    }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {  // 128 columns of tensor memory: the fp32 accumulator, one lane per row
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_addr(&tmem_base))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    __syncthreads();
+    float *cur = sw, *nxt = sw2;
+    for (int d = 1; d < L; d <<= 1) {
+        nxt[tid] = tid + d < L ? __fmul_rn(cur[tid], cur[tid + d]) : cur[tid];
+        __syncthreads();
+        float *tmp = cur;
+        cur = nxt;
+        nxt = tmp;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // w o U in fp32, split into two bf16 parts, into the A operands
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+        const int s = task_s(it), q = task_q(it);
+        const float ws = cur[s], ds = sdt[s];
+        const __nv_bfloat16 *xv = reinterpret_cast<const __nv_bfloat16 *>(&xr[it]);
+        uint32_t p1[4], p2[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            uint32_t w1[2], w2[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float av = __fmul_rn(ws, ssm_input_scale(ds, __bfloat162float(xv[e + k])));
+                const __nv_bfloat16 b1 = __float2bfloat16_rn(av);
+                w1[k] = bf16_bits(b1);
+                w2[k] = bf16_bits(__float2bfloat16_rn(av - __bfloat162float(b1)));
+            }
+            p1[e / 2] = w1[0] | (w1[1] << 16);
+            p2[e / 2] = w2[0] | (w2[1] << 16);
+        }
+        const uint32_t off = tc_operand_off(s, q * 8);
+        *reinterpret_cast<uint4 *>(sbytes + TCLay::kA + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+        *reinterpret_cast<uint4 *>(sbytes + TCLay::kA + TCLay::kPart + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+    }
+    fence_proxy_async_smem();  // the operands written by the threads, visible to the tensor cores
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t taddr = tmem_base;
+    if (tid == 0) {
+        const uint32_t abase = smem_addr(sbytes + TCLay::kA), bbase = smem_addr(sbytes + TCLay::kB);
+        for (int part = 0; part < kTCParts; ++part)
+            for (int kk = 0; kk < L / 16; ++kk)
+                tc_mma(taddr, tc_desc(abase + part * TCLay::kPart + kk * 4096), tc_desc(bbase + kk * 4096),
+                       (part | kk) != 0 ? 1u : 0u);
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_addr(&bar))
+                     : "memory");
+    }
+    const bool ok = mbar_wait_bounded(&bar, 0u);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok) {
+        const int r = warp * 32 + lane;
+        float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0 + r) * 128;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+            uint32_t u[16];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+                  "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+                : "r"(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int k = 0; k < 16; k += 4)
+                *reinterpret_cast<float4 *>(out + c0 + k) = make_float4(__uint_as_float(u[k]), __uint_as_float(u[k + 1]),
+                                                                        __uint_as_float(u[k + 2]), __uint_as_float(u[k + 3]));
+        }
+    } else {  // never on a healthy device: report, wait once more for the products, then free the memory
+        if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
+        mbar_wait_bounded(&bar, 0u);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(taddr) : "memory");
 }
 
 // Chunked prefill, the pass between the chunk passes: carry the state across a
@@ -1645,6 +1834,20 @@ cudaError_t launch_cs_t(const CSArgs &a, long long ntiles, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_chunk_state_tc(const CSArgs &a, long long ntiles, cudaStream_t s) {
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || ready[dev].load(std::memory_order_relaxed) == 0) {
+        e = cudaFuncSetAttribute(ssm_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TCLay::kBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_relaxed);
+    }
+    ssm_chunk_state_tc_kernel<<<(unsigned)ntiles, 128, TCLay::kBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_state(int in_dtype, int N, const CSArgs &a, long long ntiles, cudaStream_t s) {
     if (in_dtype == SSM_BF16) {
         switch (N) {
@@ -1716,6 +1919,8 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     c1.dev_status = dev_status;
     const bool cs_ok = N <= 128 && P % kCSRows == 0 && aligned(x, 16) && aligned(B, 16) && (P * eb) % 16 == 0 &&
                        aligned(dt, eb);
+    // the tensor-memory form: bf16 inputs, N = 128, L = 128, 128-row tiles
+    const bool tc_ok = cs_ok && d->in_dtype == SSM_BF16 && N == 128 && L == 128 && P % kTCRows == 0;
     if (cs_ok) {
         CSArgs ca;
         ca.x = x;
@@ -1723,13 +1928,16 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         ca.dt = dt;
         ca.A = A;
         ca.ws = static_cast<float *>(ws);
+        ca.dev_status = dev_status;
         ca.H = (int)H;
         ca.P = (int)P;
         ca.G = (int)G;
         ca.L = L;
-        ca.ptiles = (int)(P / kCSRows);
-        const long long nt = (long long)dv.batch * H * (P / kCSRows);
-        const cudaError_t e1 = launch_chunk_state(d->in_dtype, (int)N, ca, nt, static_cast<cudaStream_t>(stream));
+        const int rows = tc_ok ? kTCRows : kCSRows;
+        ca.ptiles = (int)(P / rows);
+        const long long nt = (long long)dv.batch * H * (P / rows);
+        const cudaError_t e1 = tc_ok ? launch_chunk_state_tc(ca, nt, static_cast<cudaStream_t>(stream))
+                                     : launch_chunk_state(d->in_dtype, (int)N, ca, nt, static_cast<cudaStream_t>(stream));
         if (e1 != cudaSuccess) {
             g_last_cuda_error = (int)e1;
             return SSM_ERR_CUDA;

@@ -184,6 +184,12 @@ def test_prefill_llama_layer_shape(cuda_device):
     _prefill_case(cuda_device, 1, 32, 128, 128, 8, 2048, synth.BF16, seed=461)
 
 
+def test_prefill_tensor_memory_chunk_states(cuda_device):
+    """A shape whose chunk states take the tensor-memory (tcgen05) pass: bf16,
+    N = 128, 128-token chunks, two 128-row tiles per head (P = 256)."""
+    _prefill_case(cuda_device, 2, 16, 256, 128, 4, 1024, synth.BF16, seed=462)
+
+
 def test_prefill_then_speculative_round(cuda_device):
     """Prefill a prompt, then verify + commit K drafts from the cached state:
     the same as the oracle over the prompt followed by the drafts."""
