@@ -1244,25 +1244,26 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
 // inputs, N = 128, L = 128 and 128-row tiles: one CTA computes
 // S[p][n] = sum_s (w_s u_s[p]) B_s[n] for 128 rows of one head of one chunk
 // as an M = 128, N = 128, K = 128 product accumulated in tensor memory.
-//  * Operands in shared memory, MN-major, no swizzle: 8 (token) x 16-byte
-//    core matrices, row- or state-channel-contiguous as x and B arrive, so
-//    nothing is transposed: element (token s, index i) of an operand sits at
-//    byte (i / 8) * 128 + (s / 8) * 2048 + (s % 8) * 16 + (i % 8) * 2; the
-//    descriptor's leading offset is the token stride (2048), its stride
-//    offset the index stride (128).
+//  * Operands in shared memory, K-major (token index contiguous), no swizzle:
+//    8-row x 16-byte core matrices; element (row r, token s) of an operand
+//    sits at byte (r / 8) * 2048 + (s / 8) * 128 + (r % 8) * 16 + (s % 8) * 2;
+//    the descriptor's leading offset is the token stride (128), its stride
+//    offset the row stride (2048). x and B arrive row-contiguous per token,
+//    so each thread transposes one 8 x 8 block of each in registers.
 //  * w o U is formed in fp32 by the arithmetic of ssm_chunk_state_kernel and
 //    split into two bf16 parts a1 + a2 (a1 = bf16(a), a2 = bf16(a - a1):
 //    16 significant bits, |a - a1 - a2| <= 2^-18 |a|); B is bf16 and exact.
 //    2 parts x 8 MMAs of K = 16 tokens (tcgen05.mma kind::f16, bf16 x bf16,
 //    fp32 accumulation), issued by one thread; tcgen05.commit signals an
-//    mbarrier, waited on with a time limit. 97 KB of shared memory: two CTAs
-//    per SM, so one CTA's loads overlap the other's products.
-//  * Row p of the accumulator is tensor-memory lane p: warp w reads rows
-//    32w .. 32w + 31 with tcgen05.ld and writes them to the workspace.
+//    mbarrier, waited on with a time limit. 97.5 KB of shared memory: two
+//    CTAs of 256 threads per SM.
+//  * Row p of the accumulator is tensor-memory lane p: warps w and w + 4
+//    read rows 32 (w % 4) .. + 31 (each half of the columns) with tcgen05.ld.
 constexpr int kTCRows = 128;
 constexpr int kTCParts = 2;
+constexpr int kTCThreads = 256;
 struct TCLay {
-    static constexpr int kPart = 128 * 128 * 2;       // one bf16 operand: 128 tokens x 128 indices
+    static constexpr int kPart = 128 * 128 * 2;       // one bf16 operand: 128 rows x 128 tokens
     static constexpr int kA = 0;                      // w o U parts a1, a2
     static constexpr int kB = kA + kTCParts * kPart;  // B
     static constexpr int kW = kB + kPart;
@@ -1271,33 +1272,55 @@ struct TCLay {
     static constexpr int kBytes = kDt + 128 * 4;
 };
 
+// MN-major layout (token s, index i): 8 (token) x 16-byte core matrices, index-contiguous.
 __device__ __forceinline__ uint32_t tc_operand_off(int s, int i) {
     return (uint32_t)((i >> 3) * 128 + (s >> 3) * 2048 + (s & 7) * 16 + (i & 7) * 2);
 }
 
-// Shared-memory matrix descriptor: start address, leading byte offset (token
-// direction) 2048, stride byte offset (index direction) 128, version 1, no swizzle.
-__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(2048u >> 4) << 16) | ((uint64_t)(128u >> 4) << 32) |
+// K-major operand: row r (M or N index), token (K index) k.
+__device__ __forceinline__ uint32_t tck_off(int r, int k) {
+    return (uint32_t)((r >> 3) * 2048 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+__device__ __forceinline__ uint64_t tck_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(2048u >> 4) << 32) |
            ((uint64_t)1 << 46);
 }
+// kind::f16, fp32 accumulator, bf16 A and B, both K-major, M = N = 128.
+constexpr uint32_t kTCIdescKK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// MN-major, N = 128, M = 128.
-constexpr uint32_t kTCIdesc =
-    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-
-__device__ __forceinline__ void tc_mma(uint32_t taddr, uint64_t ad, uint64_t bd, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma_i(uint32_t taddr, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(taddr),
-        "l"(ad), "l"(bd), "r"(kTCIdesc), "r"(accumulate)
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
         : "memory");
 }
-
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&f)[16]) {
+    uint32_t u[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(u[i]);
+}
 __device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 v) { return (uint32_t)__bfloat16_as_ushort(v); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return bf16_bits(__float2bfloat16_rn(lo)) | (bf16_bits(__float2bfloat16_rn(hi)) << 16);
+}
+// 16-bit element e (0..7) of an 8-element row held as a uint4
+__device__ __forceinline__ uint32_t u16_at(const uint4 &r, int e) {
+    const uint32_t w = e < 4 ? (e < 2 ? r.x : r.y) : (e < 6 ? r.z : r.w);
+    return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
 
-__global__ void __launch_bounds__(128, 2) ssm_chunk_state_tc_kernel(const CSArgs a) {
+__global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const CSArgs a) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t tmem_base;
     unsigned char *sbytes = reinterpret_cast<unsigned char *>(ssm_smem);
@@ -1316,25 +1339,17 @@ __global__ void __launch_bounds__(128, 2) ssm_chunk_state_tc_kernel(const CSArgs
     const __nv_bfloat16 *Bp = static_cast<const __nv_bfloat16 *>(a.B);
     const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
 
-    // A warp task: 8 consecutive tokens x 4 consecutive 16-byte index chunks, lane (token lane % 8, chunk
-    // lane / 8): a warp's shared stores fill four whole 128-byte lines, and its global reads are 64 bytes
-    // of each of 8 rows. 64 tasks, 16 per warp.
-    auto task_s = [&](int it) { return ((warp + 4 * it) & 15) * 8 + (lane & 7); };
-    auto task_q = [&](int it) { return ((warp + 4 * it) >> 4) * 4 + (lane >> 3); };
-    // B straight into its operand layout, 16 bytes at a time
-#pragma unroll 4
-    for (int it = 0; it < 16; ++it) {
-        const int s = task_s(it), q = task_q(it);
-        cp_async16(sbytes + TCLay::kB + tc_operand_off(s, q * 8), Bp + ((v * L + s) * a.G + gi) * 128LL + q * 8);
-    }
-    // this thread's x vectors, loaded ahead of the product tree
-    uint4 xr[16];
+    // this thread's 8 x 8 blocks: tokens s0 .. s0+7 of rows p0 .. p0+7 (x) and of columns p0 .. p0+7 (B)
+    const int bp = tid & 15, bs = tid >> 4, p0 = bp * 8, s0 = bs * 8;
+    uint4 xr[8], br[8];
 #pragma unroll
-    for (int it = 0; it < 16; ++it)
-        xr[it] = __ldg(reinterpret_cast<const uint4 *>(x + ((v * L + task_s(it)) * a.H + h) * (long long)a.P + row0 +
-                                                       task_q(it) * 8));
+    for (int i = 0; i < 8; ++i) {
+        const long long bt = v * L + s0 + i;
+        xr[i] = __ldg(reinterpret_cast<const uint4 *>(x + (bt * a.H + h) * (long long)a.P + row0 + p0));
+        br[i] = __ldg(reinterpret_cast<const uint4 *>(Bp + (bt * a.G + gi) * 128LL + p0));
+    }
     // dt and the suffix products w_s = prod_{r > s} Abar_r (the product tree of ssm_chunk_state_kernel)
-    {
+    if (tid < L) {
         const float d = ld1(dtp + (v * L + tid) * a.H + h);
         sdt[tid] = d;
         sw[tid] = tid + 1 < L ? ssm_decay(ld1(dtp + (v * L + tid + 1) * a.H + h), Ah) : 1.f;
@@ -1348,39 +1363,50 @@ __global__ void __launch_bounds__(128, 2) ssm_chunk_state_tc_kernel(const CSArgs
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // B transposed into its operand (row n = p0 + j, tokens s0 .. s0+7); row order rotated per lane
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int j = (k + lane) & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) w[e / 2] = u16_at(br[e], j) | (u16_at(br[e + 1], j) << 16);
+        *reinterpret_cast<uint4 *>(sbytes + TCLay::kB + tck_off(p0 + j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
     __syncthreads();
     float *cur = sw, *nxt = sw2;
     for (int d = 1; d < L; d <<= 1) {
-        nxt[tid] = tid + d < L ? __fmul_rn(cur[tid], cur[tid + d]) : cur[tid];
+        if (tid < L) nxt[tid] = tid + d < L ? __fmul_rn(cur[tid], cur[tid + d]) : cur[tid];
         __syncthreads();
         float *tmp = cur;
         cur = nxt;
         nxt = tmp;
     }
-    cp_async_wait_all();
-    __syncthreads();
-
-    // w o U in fp32, split into two bf16 parts, into the A operands
+    // w o U in fp32, split into two bf16 parts, transposed into the A operands (row p0 + j)
+    float wsv[8], dsv[8];
 #pragma unroll
-    for (int it = 0; it < 16; ++it) {
-        const int s = task_s(it), q = task_q(it);
-        const float ws = cur[s], ds = sdt[s];
-        const __nv_bfloat16 *xv = reinterpret_cast<const __nv_bfloat16 *>(&xr[it]);
+    for (int i = 0; i < 8; ++i) {
+        wsv[i] = cur[s0 + i];
+        dsv[i] = sdt[s0 + i];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int j = (k + lane) & 7;
         uint32_t p1[4], p2[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
             uint32_t w1[2], w2[2];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const float av = __fmul_rn(ws, ssm_input_scale(ds, __bfloat162float(xv[e + k])));
+            for (int q = 0; q < 2; ++q) {
+                const float xv = __uint_as_float(u16_at(xr[e + q], j) << 16);  // bf16 -> fp32, exact
+                const float av = __fmul_rn(wsv[e + q], ssm_input_scale(dsv[e + q], xv));
                 const __nv_bfloat16 b1 = __float2bfloat16_rn(av);
-                w1[k] = bf16_bits(b1);
-                w2[k] = bf16_bits(__float2bfloat16_rn(av - __bfloat162float(b1)));
+                w1[q] = bf16_bits(b1);
+                w2[q] = bf16_bits(__float2bfloat16_rn(av - __bfloat162float(b1)));
             }
             p1[e / 2] = w1[0] | (w1[1] << 16);
             p2[e / 2] = w2[0] | (w2[1] << 16);
         }
-        const uint32_t off = tc_operand_off(s, q * 8);
+        const uint32_t off = tck_off(p0 + j, s0);
         *reinterpret_cast<uint4 *>(sbytes + TCLay::kA + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
         *reinterpret_cast<uint4 *>(sbytes + TCLay::kA + TCLay::kPart + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
     }
@@ -1393,39 +1419,283 @@ __global__ void __launch_bounds__(128, 2) ssm_chunk_state_tc_kernel(const CSArgs
         const uint32_t abase = smem_addr(sbytes + TCLay::kA), bbase = smem_addr(sbytes + TCLay::kB);
         for (int part = 0; part < kTCParts; ++part)
             for (int kk = 0; kk < L / 16; ++kk)
-                tc_mma(taddr, tc_desc(abase + part * TCLay::kPart + kk * 4096), tc_desc(bbase + kk * 4096),
-                       (part | kk) != 0 ? 1u : 0u);
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                         smem_addr(&bar))
-                     : "memory");
+                tc_mma_i(taddr, tck_desc(abase + part * TCLay::kPart + kk * 256), tck_desc(bbase + kk * 256),
+                         kTCIdescKK, (part | kk) != 0 ? 1u : 0u);
+        tc_commit(&bar);
     }
     const bool ok = mbar_wait_bounded(&bar, 0u);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok) {
-        const int r = warp * 32 + lane;
-        float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0 + r) * 128;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t u[16];
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
-                  "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
-                : "r"(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-            for (int k = 0; k < 16; k += 4)
-                *reinterpret_cast<float4 *>(out + c0 + k) = make_float4(__uint_as_float(u[k]), __uint_as_float(u[k + 1]),
-                                                                        __uint_as_float(u[k + 2]), __uint_as_float(u[k + 3]));
-        }
-    } else {  // never on a healthy device: report, wait once more for the products, then free the memory
+    if (__syncthreads_or(!ok)) {  // never on a healthy device: report, wait once more for the products
         if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
         mbar_wait_bounded(&bar, 0u);
+    } else {
+        const int r = (warp & 3) * 32 + lane, ch = (warp >> 2) * 64;
+        float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0 + r) * 128;
+        const uint32_t trow = taddr + ((uint32_t)((warp & 3) * 32) << 16);
+#pragma unroll 1
+        for (int c0 = ch; c0 < ch + 64; c0 += 16) {
+            float f[16];
+            tc_ld16(trow + c0, f);
+#pragma unroll
+            for (int k = 0; k < 16; k += 4)
+                *reinterpret_cast<float4 *>(out + c0 + k) = make_float4(f[k], f[k + 1], f[k + 2], f[k + 3]);
+        }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(taddr) : "memory");
+}
+
+// Chunked prefill, output pass on the tensor cores (tcgen05), for the shapes
+// of ssm_chunk_state_tc_kernel: y of every token of a 128-token chunk from the
+// state H0 the chunk starts from, in the chunked (attention-like) form of the
+// recurrence,
+//     y_t = w_t (C_t . H0) + sum_{s<=t} exp(A (cs_t - cs_s)) dt_s (C_t . B_s) x_s + D x_t,
+//     cs_t = sum_{r<=t} dt_r,   w_t = exp(A cs_t),
+// for 128 rows p of one head. Three products accumulate in tensor memory:
+//   Yi = C H0^T   (128 tokens x 128 rows, over 128 state channels; H0 split
+//                  into two bf16 parts, C exact),
+//   G  = C B^T    (128 x 128 tokens; bf16, exact inputs),
+//   Yc = M X      (M[t][s] = G[t][s] exp(A (cs_t - cs_s)) dt_s for s <= t,
+//                  else 0, split into two bf16 parts; x exact),
+// and y = w_t Yi + Yc + D x. One CTA of 256 threads per (chunk, head,
+// 128-row tile); row t of every accumulator is tensor-memory lane t, read by
+// warps w and w + 4 (each half of the columns). Every operand is K-major
+// (leading offset 128, the K-direction stride; stride offset 2048): on this
+// hardware a no-swizzle MN-major operand ran about ten times slower per
+// instruction. x arrives row-contiguous per token, so each thread transposes
+// one 8 x 8 block in registers; an MN-major copy of x serves the D x term.
+struct OutArgs {
+    const void *x, *B, *C, *dt;  // [batch][T] layouts; chunk v = tokens v*128 .. v*128 + 127
+    const float *A, *D;
+    const float *ws;             // [chunks][H][P][N]: the state each chunk starts from
+    const int32_t *vslot;        // nullable: chunk v writes no y where vslot[v] < 0
+    float *y;                    // [batch][T][H][P]
+    uint32_t *dev_status;
+    int H, P, G, ptiles;
+};
+
+constexpr int kOutThreads = 256;
+struct OutLay {
+    static constexpr int kOp = 128 * 128 * 2;  // one bf16 operand, 128 x 128
+    static constexpr int kC = 0;               // C    K-major [t][n]   (later: M part 1)
+    static constexpr int kB = kC + kOp;        // B    K-major [s][n]   (later: M part 2)
+    static constexpr int kH1 = kB + kOp;       // H0 part 1, K-major [p][n]
+    static constexpr int kH2 = kH1 + kOp;      // H0 part 2
+    static constexpr int kXk = kH2 + kOp;      // x    K-major [p][s]
+    static constexpr int kXm = kXk + kOp;      // x    MN-major (token s, row p), for D x
+    static constexpr int kCs = kXm + kOp;      // float[128] cs_t
+    static constexpr int kDt = kCs + 512;      // float[128] dt_t
+    static constexpr int kBytes = kDt + 512;
+};
+
+__global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const OutArgs a) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ float wsum[4];
+    unsigned char *sb = reinterpret_cast<unsigned char *>(ssm_smem);
+    float *scs = sm<float>(OutLay::kCs), *sdt = sm<float>(OutLay::kDt);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long tile = blockIdx.x;
+    const int ptile = (int)(tile % a.ptiles);
+    const long long vh = tile / a.ptiles;
+    const int h = (int)(vh % a.H);
+    const long long v = vh / a.H;
+    const int gi = h / (a.H / a.G);
+    const int row0 = ptile * 128;
+    const float Ah = __ldg(a.A + h), Dh = __ldg(a.D + h);
+    const bool write_y = a.vslot == nullptr || __ldg(a.vslot + v) >= 0;
+    const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(a.x);
+    const __nv_bfloat16 *Bg = static_cast<const __nv_bfloat16 *>(a.B);
+    const __nv_bfloat16 *Cg = static_cast<const __nv_bfloat16 *>(a.C);
+    const __nv_bfloat16 *dtg = static_cast<const __nv_bfloat16 *>(a.dt);
+    // warp task (8 consecutive rows x 4 consecutive 16-byte chunks), 8 per warp: conflict-free stores
+    auto task_r = [&](int it) { return ((warp + 8 * it) & 15) * 8 + (lane & 7); };
+    auto task_q = [&](int it) { return ((warp + 8 * it) >> 4) * 4 + (lane >> 3); };
+
+    // C and B (K-major, row = token): straight into their operand layouts
+#pragma unroll 4
+    for (int it = 0; it < 8; ++it) {
+        const int t = task_r(it), q = task_q(it);
+        const long long bt = v * 128 + t;
+        cp_async16(sb + OutLay::kC + tck_off(t, q * 8), Cg + (bt * a.G + gi) * 128LL + q * 8);
+        cp_async16(sb + OutLay::kB + tck_off(t, q * 8), Bg + (bt * a.G + gi) * 128LL + q * 8);
+    }
+    // this thread's 8 x 8 block of x (tokens s0 .. s0+7, rows p0 .. p0+7) and H0 chunks: all loads in flight
+    const int bp = tid & 15, bs = tid >> 4, p0 = bp * 8, s0 = bs * 8;
+    uint4 xr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        xr[i] = __ldg(reinterpret_cast<const uint4 *>(xg + ((v * 128 + s0 + i) * a.H + h) * (long long)a.P + row0 + p0));
+    const float *H0 = a.ws + ((v * a.H + h) * (long long)a.P + row0) * 128;
+    float4 hr[8][2];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const float *src = H0 + task_r(it) * 128 + task_q(it) * 8;
+        hr[it][0] = __ldcs(reinterpret_cast<const float4 *>(src));
+        hr[it][1] = __ldcs(reinterpret_cast<const float4 *>(src + 4));
+    }
+    // dt and its inclusive prefix sum over the chunk (warps 0..3: warp scans, then the warps' totals in order)
+    float dcs = 0.f;
+    if (tid < 128) {
+        const float d = ld1(dtg + (v * 128 + tid) * a.H + h);
+        sdt[tid] = d;
+        dcs = d;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, dcs, o);
+            if (lane >= o) dcs += u;
+        }
+        if (lane == 31) wsum[warp] = dcs;
+    }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {  // 512 columns: Yi at 0, G at 128, Yc at 256
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_addr(&tmem_base))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // x: the MN-major copy (rows of the block as they are) and the K-major copy (the block transposed);
+    // the row order is rotated per thread to spread the stores over the banks
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = (k + bp) & 7;
+        *reinterpret_cast<uint4 *>(sb + OutLay::kXm + tc_operand_off(s0 + i, p0)) = xr[i];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int j = (k + lane) & 7;  // row p0 + j of the K-major copy: element j of each token row
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) w[e / 2] = u16_at(xr[e], j) | (u16_at(xr[e + 1], j) << 16);
+        *reinterpret_cast<uint4 *>(sb + OutLay::kXk + tck_off(p0 + j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // H0 split into two bf16 parts (K-major, row = p)
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int pr = task_r(it), q = task_q(it);
+        const float f[8] = {hr[it][0].x, hr[it][0].y, hr[it][0].z, hr[it][0].w,
+                            hr[it][1].x, hr[it][1].y, hr[it][1].z, hr[it][1].w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat16 a0 = __float2bfloat16_rn(f[e]), a1 = __float2bfloat16_rn(f[e + 1]);
+            hi[e / 2] = bf16_bits(a0) | (bf16_bits(a1) << 16);
+            lo[e / 2] = pack_bf16x2(f[e] - __bfloat162float(a0), f[e + 1] - __bfloat162float(a1));
+        }
+        const uint32_t off = tck_off(pr, q * 8);
+        *reinterpret_cast<uint4 *>(sb + OutLay::kH1 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(sb + OutLay::kH2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    __syncthreads();  // wsum
+    if (tid < 128) {
+        float base = 0.f;
+        for (int w = 0; w < warp; ++w) base += wsum[w];
+        scs[tid] = base + dcs;
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t taddr = tmem_base;
+    const uint32_t base = smem_addr(sb);
+    if (tid == 0) {
+        for (int kk = 0; kk < 8; ++kk)  // Yi = C H0^T, both parts
+            tc_mma_i(taddr, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kH1 + kk * 256),
+                     kTCIdescKK, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+            tc_mma_i(taddr, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kH2 + kk * 256),
+                     kTCIdescKK, 1u);
+        for (int kk = 0; kk < 8; ++kk)  // G = C B^T
+            tc_mma_i(taddr + 128, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kB + kk * 256),
+                     kTCIdescKK, kk > 0 ? 1u : 0u);
+        tc_commit(&bar);
+    }
+    bool ok = mbar_wait_bounded(&bar, 0u);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int t = (warp & 3) * 32 + lane;  // this thread's token (tensor-memory lane)
+    const int ch = (warp >> 2) * 64;       // its half of the columns
+    const uint32_t trow = taddr + ((uint32_t)((warp & 3) * 32) << 16);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
+        mbar_wait_bounded(&bar, 0u);
+    } else {
+        // M = mask(G) o decay o dt, split into two bf16 parts, into the freed C / B space (K-major, row = t)
+        const float cst = scs[t];
+#pragma unroll 1
+        for (int c = ch; c < ch + 64; c += 16) {
+            float g[16];
+            tc_ld16(trow + 128 + c, g);
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                float m[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int sx = c + e + k;
+                    m[k] = sx <= t ? __fmul_rn(__fmul_rn(g[e + k], expf(__fmul_rn(Ah, cst - scs[sx]))), sdt[sx]) : 0.f;
+                }
+                const __nv_bfloat16 b0 = __float2bfloat16_rn(m[0]), b1 = __float2bfloat16_rn(m[1]);
+                hi[e / 2] = bf16_bits(b0) | (bf16_bits(b1) << 16);
+                lo[e / 2] = pack_bf16x2(m[0] - __bfloat162float(b0), m[1] - __bfloat162float(b1));
+            }
+            *reinterpret_cast<uint4 *>(sb + OutLay::kC + tck_off(t, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kC + tck_off(t, c + 8)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kB + tck_off(t, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kB + tck_off(t, c + 8)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+        fence_proxy_async_smem();
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (tid == 0) {
+            for (int kk = 0; kk < 8; ++kk)  // Yc = M X, both parts of M
+                tc_mma_i(taddr + 256, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kXk + kk * 256),
+                         kTCIdescKK, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_i(taddr + 256, tck_desc(base + OutLay::kB + kk * 256), tck_desc(base + OutLay::kXk + kk * 256),
+                         kTCIdescKK, 1u);
+            tc_commit(&bar);
+        }
+        ok = mbar_wait_bounded(&bar, 1u);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
+            mbar_wait_bounded(&bar, 1u);
+        } else if (write_y) {
+            // y = w_t Yi + Yc + D x, this thread's half of row t
+            const float wt = expf(__fmul_rn(Ah, cst));
+            float *yrow = a.y + ((v * 128 + t) * a.H + h) * (long long)a.P + row0;
+#pragma unroll 1
+            for (int c0 = ch; c0 < ch + 64; c0 += 16) {
+                float yi[16], yc[16];
+                tc_ld16(trow + c0, yi);
+                tc_ld16(trow + 256 + c0, yc);
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(sb + OutLay::kXm + tc_operand_off(t, c0));
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(sb + OutLay::kXm + tc_operand_off(t, c0 + 8));
+                const __nv_bfloat16 *xa = reinterpret_cast<const __nv_bfloat16 *>(&x0);
+                const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(&x1);
+#pragma unroll
+                for (int k = 0; k < 16; k += 4) {
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float xv = __bfloat162float(k + e < 8 ? xa[k + e] : xb[k + e - 8]);
+                        o[e] = __fmaf_rn(wt, yi[k + e], yc[k + e]) + __fmul_rn(Dh, xv);
+                    }
+                    __stcs(reinterpret_cast<float4 *>(yrow + c0 + k), make_float4(o[0], o[1], o[2], o[3]));
+                }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(taddr) : "memory");
 }
 
 // Chunked prefill, the pass between the chunk passes: carry the state across a
@@ -1844,7 +2114,21 @@ cudaError_t launch_chunk_state_tc(const CSArgs &a, long long ntiles, cudaStream_
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_relaxed);
     }
-    ssm_chunk_state_tc_kernel<<<(unsigned)ntiles, 128, TCLay::kBytes, s>>>(a);
+    ssm_chunk_state_tc_kernel<<<(unsigned)ntiles, kTCThreads, TCLay::kBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_out_tc(const OutArgs &a, long long ntiles, cudaStream_t s) {
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || ready[dev].load(std::memory_order_relaxed) == 0) {
+        e = cudaFuncSetAttribute(ssm_chunk_out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, OutLay::kBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_relaxed);
+    }
+    ssm_chunk_out_tc_kernel<<<(unsigned)ntiles, kOutThreads, OutLay::kBytes, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -1973,6 +2257,24 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         return SSM_ERR_CUDA;
     }
 
+    if (tc_ok && aligned(C, 16) && aligned(y, 16)) {  // the chunked output form on the tensor cores
+        OutArgs oa;
+        oa.x = x; oa.B = B; oa.C = C; oa.dt = dt;
+        oa.A = A; oa.D = D;
+        oa.ws = static_cast<const float *>(ws);
+        oa.vslot = vslot;
+        oa.y = y;
+        oa.dev_status = dev_status;
+        oa.H = (int)H; oa.P = (int)P; oa.G = (int)G;
+        oa.ptiles = (int)(P / kTCRows);
+        const cudaError_t e3 = launch_chunk_out_tc(oa, (long long)dv.batch * H * (P / kTCRows),
+                                                   static_cast<cudaStream_t>(stream));
+        if (e3 != cudaSuccess) {
+            g_last_cuda_error = (int)e3;
+            return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
     Call c3{};
     c3.flavour = kVerify;
     c3.state_in = static_cast<const float *>(ws);
