@@ -1460,12 +1460,16 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
 //   Yc = M X      (M[t][s] = G[t][s] exp(A (cs_t - cs_s)) dt_s for s <= t,
 //                  else 0, split into two bf16 parts; x exact),
 // and y = w_t Yi + Yc + D x. One CTA of 256 threads per (chunk, head,
-// 128-row tile); row t of every accumulator is tensor-memory lane t, read by
-// warps w and w + 4 (each half of the columns). Every operand is K-major
-// (leading offset 128, the K-direction stride; stride offset 2048): on this
-// hardware a no-swizzle MN-major operand ran about ten times slower per
-// instruction. x arrives row-contiguous per token, so each thread transposes
-// one 8 x 8 block in registers; an MN-major copy of x serves the D x term.
+// 128-row tile), two CTAs per SM: three 32 KB operand buffers are reused
+// phase by phase (C and B, then the low part of H0 over B, then M over H0
+// and C with x over B), and Yc accumulates in G's tensor-memory columns once
+// G has been read, so a CTA needs 97 KB of shared memory and 256 columns.
+// Row t of every accumulator is tensor-memory lane t, read by warps w and
+// w + 4 (each half of the columns). Every operand is K-major (leading offset
+// 128, the K-direction stride; stride offset 2048): on this hardware a
+// no-swizzle MN-major operand ran about ten times slower per instruction.
+// x arrives row-contiguous per token, so each thread transposes one 8 x 8
+// block in registers; the D x term reads x again from L2.
 struct OutArgs {
     const void *x, *B, *C, *dt;  // [batch][T] layouts; chunk v = tokens v*128 .. v*128 + 127
     const float *A, *D;
@@ -1478,19 +1482,16 @@ struct OutArgs {
 
 constexpr int kOutThreads = 256;
 struct OutLay {
-    static constexpr int kOp = 128 * 128 * 2;  // one bf16 operand, 128 x 128
-    static constexpr int kC = 0;               // C    K-major [t][n]   (later: M part 1)
-    static constexpr int kB = kC + kOp;        // B    K-major [s][n]   (later: M part 2)
-    static constexpr int kH1 = kB + kOp;       // H0 part 1, K-major [p][n]
-    static constexpr int kH2 = kH1 + kOp;      // H0 part 2
-    static constexpr int kXk = kH2 + kOp;      // x    K-major [p][s]
-    static constexpr int kXm = kXk + kOp;      // x    MN-major (token s, row p), for D x
-    static constexpr int kCs = kXm + kOp;      // float[128] cs_t
+    static constexpr int kOp = 128 * 128 * 2;  // one bf16 operand, 128 x 128, K-major
+    static constexpr int kP0 = 0;              // C, later M part 2
+    static constexpr int kP1 = kP0 + kOp;      // B, then H0 part 2, then x (row p, token s)
+    static constexpr int kP2 = kP1 + kOp;      // H0 part 1, later M part 1
+    static constexpr int kCs = kP2 + kOp;      // float[128] cs_t
     static constexpr int kDt = kCs + 512;      // float[128] dt_t
     static constexpr int kBytes = kDt + 512;
 };
 
-__global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const OutArgs a) {
+__global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const OutArgs a) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t tmem_base;
     __shared__ float wsum[4];
@@ -1519,22 +1520,28 @@ __global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const 
     for (int it = 0; it < 8; ++it) {
         const int t = task_r(it), q = task_q(it);
         const long long bt = v * 128 + t;
-        cp_async16(sb + OutLay::kC + tck_off(t, q * 8), Cg + (bt * a.G + gi) * 128LL + q * 8);
-        cp_async16(sb + OutLay::kB + tck_off(t, q * 8), Bg + (bt * a.G + gi) * 128LL + q * 8);
+        cp_async16(sb + OutLay::kP0 + tck_off(t, q * 8), Cg + (bt * a.G + gi) * 128LL + q * 8);
+        cp_async16(sb + OutLay::kP1 + tck_off(t, q * 8), Bg + (bt * a.G + gi) * 128LL + q * 8);
     }
-    // this thread's 8 x 8 block of x (tokens s0 .. s0+7, rows p0 .. p0+7) and H0 chunks: all loads in flight
-    const int bp = tid & 15, bs = tid >> 4, p0 = bp * 8, s0 = bs * 8;
-    uint4 xr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        xr[i] = __ldg(reinterpret_cast<const uint4 *>(xg + ((v * 128 + s0 + i) * a.H + h) * (long long)a.P + row0 + p0));
+    // H0 (row p, K-major): high part into its operand now, low part kept packed for the second product
     const float *H0 = a.ws + ((v * a.H + h) * (long long)a.P + row0) * 128;
-    float4 hr[8][2];
+    uint4 hlo[8];
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const float *src = H0 + task_r(it) * 128 + task_q(it) * 8;
-        hr[it][0] = __ldcs(reinterpret_cast<const float4 *>(src));
-        hr[it][1] = __ldcs(reinterpret_cast<const float4 *>(src + 4));
+        const float4 f0 = __ldcs(reinterpret_cast<const float4 *>(src));
+        const float4 f1 = __ldcs(reinterpret_cast<const float4 *>(src + 4));
+        const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat16 a0 = __float2bfloat16_rn(f[e]), a1 = __float2bfloat16_rn(f[e + 1]);
+            hi[e / 2] = bf16_bits(a0) | (bf16_bits(a1) << 16);
+            lo[e / 2] = pack_bf16x2(f[e] - __bfloat162float(a0), f[e + 1] - __bfloat162float(a1));
+        }
+        *reinterpret_cast<uint4 *>(sb + OutLay::kP2 + tck_off(task_r(it), task_q(it) * 8)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        hlo[it] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     // dt and its inclusive prefix sum over the chunk (warps 0..3: warp scans, then the warps' totals in order)
     float dcs = 0.f;
@@ -1553,42 +1560,10 @@ __global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const 
         mbar_init(&bar, 1);
         fence_barrier_init();
     }
-    if (warp == 0) {  // 512 columns: Yi at 0, G at 128, Yc at 256
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_addr(&tmem_base))
+    if (warp == 0) {  // 256 columns: Yi at 0; G at 128, later Yc
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_addr(&tmem_base))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    // x: the MN-major copy (rows of the block as they are) and the K-major copy (the block transposed);
-    // the row order is rotated per thread to spread the stores over the banks
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int i = (k + bp) & 7;
-        *reinterpret_cast<uint4 *>(sb + OutLay::kXm + tc_operand_off(s0 + i, p0)) = xr[i];
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int j = (k + lane) & 7;  // row p0 + j of the K-major copy: element j of each token row
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) w[e / 2] = u16_at(xr[e], j) | (u16_at(xr[e + 1], j) << 16);
-        *reinterpret_cast<uint4 *>(sb + OutLay::kXk + tck_off(p0 + j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    // H0 split into two bf16 parts (K-major, row = p)
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int pr = task_r(it), q = task_q(it);
-        const float f[8] = {hr[it][0].x, hr[it][0].y, hr[it][0].z, hr[it][0].w,
-                            hr[it][1].x, hr[it][1].y, hr[it][1].z, hr[it][1].w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const __nv_bfloat16 a0 = __float2bfloat16_rn(f[e]), a1 = __float2bfloat16_rn(f[e + 1]);
-            hi[e / 2] = bf16_bits(a0) | (bf16_bits(a1) << 16);
-            lo[e / 2] = pack_bf16x2(f[e] - __bfloat162float(a0), f[e + 1] - __bfloat162float(a1));
-        }
-        const uint32_t off = tck_off(pr, q * 8);
-        *reinterpret_cast<uint4 *>(sb + OutLay::kH1 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(sb + OutLay::kH2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     __syncthreads();  // wsum
     if (tid < 128) {
@@ -1604,27 +1579,49 @@ __global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const 
     const uint32_t taddr = tmem_base;
     const uint32_t base = smem_addr(sb);
     if (tid == 0) {
-        for (int kk = 0; kk < 8; ++kk)  // Yi = C H0^T, both parts
-            tc_mma_i(taddr, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kH1 + kk * 256),
-                     kTCIdescKK, kk > 0 ? 1u : 0u);
-        for (int kk = 0; kk < 8; ++kk)
-            tc_mma_i(taddr, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kH2 + kk * 256),
-                     kTCIdescKK, 1u);
         for (int kk = 0; kk < 8; ++kk)  // G = C B^T
-            tc_mma_i(taddr + 128, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kB + kk * 256),
+            tc_mma_i(taddr + 128, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
+                     kTCIdescKK, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)  // Yi = C H0^T, high part
+            tc_mma_i(taddr, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP2 + kk * 256),
                      kTCIdescKK, kk > 0 ? 1u : 0u);
         tc_commit(&bar);
     }
+    // this thread's 8 x 8 block of x (tokens s0 .. s0+7, rows p0 .. p0+7), loaded while the products run
+    const int bp = tid & 15, bs = tid >> 4, p0 = bp * 8, s0 = bs * 8;
+    uint4 xr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        xr[i] = __ldg(reinterpret_cast<const uint4 *>(xg + ((v * 128 + s0 + i) * a.H + h) * (long long)a.P + row0 + p0));
     bool ok = mbar_wait_bounded(&bar, 0u);
+    int phase = 1;
+    if (!__syncthreads_or(!ok)) {
+        // B is no longer read: the low part of H0 takes its place; Yi += C H0^T, low part
+#pragma unroll
+        for (int it = 0; it < 8; ++it)
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP1 + tck_off(task_r(it), task_q(it) * 8)) = hlo[it];
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_i(taddr, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
+                         kTCIdescKK, 1u);
+            tc_commit(&bar);
+        }
+        ok = mbar_wait_bounded(&bar, 1u);
+        phase = 2;
+    }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const int t = (warp & 3) * 32 + lane;  // this thread's token (tensor-memory lane)
     const int ch = (warp >> 2) * 64;       // its half of the columns
     const uint32_t trow = taddr + ((uint32_t)((warp & 3) * 32) << 16);
     if (__syncthreads_or(!ok)) {
         if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
-        mbar_wait_bounded(&bar, 0u);
+        mbar_wait_bounded(&bar, (uint32_t)(phase - 1) & 1u);
     } else {
-        // M = mask(G) o decay o dt, split into two bf16 parts, into the freed C / B space (K-major, row = t)
+        // every product so far is done: M = mask(G) o decay o dt in two bf16 parts (rows t, K-major) over
+        // H0 part 1 and C; x transposed over H0 part 2 (row p, token s)
         const float cst = scs[t];
 #pragma unroll 1
         for (int c = ch; c < ch + 64; c += 16) {
@@ -1643,48 +1640,59 @@ __global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const 
                 hi[e / 2] = bf16_bits(b0) | (bf16_bits(b1) << 16);
                 lo[e / 2] = pack_bf16x2(m[0] - __bfloat162float(b0), m[1] - __bfloat162float(b1));
             }
-            *reinterpret_cast<uint4 *>(sb + OutLay::kC + tck_off(t, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(sb + OutLay::kC + tck_off(t, c + 8)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-            *reinterpret_cast<uint4 *>(sb + OutLay::kB + tck_off(t, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<uint4 *>(sb + OutLay::kB + tck_off(t, c + 8)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP2 + tck_off(t, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP2 + tck_off(t, c + 8)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP0 + tck_off(t, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP0 + tck_off(t, c + 8)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int j = (k + lane) & 7;  // row p0 + j: element j of each token row; rotated per lane
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) w[e / 2] = u16_at(xr[e], j) | (u16_at(xr[e + 1], j) << 16);
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP1 + tck_off(p0 + j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();
+        __syncthreads();  // every thread is done reading G: Yc may overwrite it
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (tid == 0) {
             for (int kk = 0; kk < 8; ++kk)  // Yc = M X, both parts of M
-                tc_mma_i(taddr + 256, tck_desc(base + OutLay::kC + kk * 256), tck_desc(base + OutLay::kXk + kk * 256),
+                tc_mma_i(taddr + 128, tck_desc(base + OutLay::kP2 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
                          kTCIdescKK, kk > 0 ? 1u : 0u);
             for (int kk = 0; kk < 8; ++kk)
-                tc_mma_i(taddr + 256, tck_desc(base + OutLay::kB + kk * 256), tck_desc(base + OutLay::kXk + kk * 256),
+                tc_mma_i(taddr + 128, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
                          kTCIdescKK, 1u);
             tc_commit(&bar);
         }
-        ok = mbar_wait_bounded(&bar, 1u);
+        // this thread's x values for D x (row t, its half of the columns), from L2 while the product runs
+        const __nv_bfloat16 *xrow = xg + ((v * 128 + t) * a.H + h) * (long long)a.P + row0 + ch;
+        uint4 xd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xd[i] = __ldg(reinterpret_cast<const uint4 *>(xrow + 8 * i));
+        ok = mbar_wait_bounded(&bar, 0u);  // third phase
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (__syncthreads_or(!ok)) {
             if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
-            mbar_wait_bounded(&bar, 1u);
+            mbar_wait_bounded(&bar, 0u);
         } else if (write_y) {
             // y = w_t Yi + Yc + D x, this thread's half of row t
             const float wt = expf(__fmul_rn(Ah, cst));
             float *yrow = a.y + ((v * 128 + t) * a.H + h) * (long long)a.P + row0;
-#pragma unroll 1
-            for (int c0 = ch; c0 < ch + 64; c0 += 16) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c0 = ch + cc * 16;
                 float yi[16], yc[16];
                 tc_ld16(trow + c0, yi);
-                tc_ld16(trow + 256 + c0, yc);
-                const uint4 x0 = *reinterpret_cast<const uint4 *>(sb + OutLay::kXm + tc_operand_off(t, c0));
-                const uint4 x1 = *reinterpret_cast<const uint4 *>(sb + OutLay::kXm + tc_operand_off(t, c0 + 8));
-                const __nv_bfloat16 *xa = reinterpret_cast<const __nv_bfloat16 *>(&x0);
-                const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(&x1);
+                tc_ld16(trow + 128 + c0, yc);
 #pragma unroll
                 for (int k = 0; k < 16; k += 4) {
                     float o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float xv = __bfloat162float(k + e < 8 ? xa[k + e] : xb[k + e - 8]);
+                        const int idx = cc * 16 + k + e;
+                        const float xv = __uint_as_float(u16_at(xd[idx >> 3], idx & 7) << 16);
                         o[e] = __fmaf_rn(wt, yi[k + e], yc[k + e]) + __fmul_rn(Dh, xv);
                     }
                     __stcs(reinterpret_cast<float4 *>(yrow + c0 + k), make_float4(o[0], o[1], o[2], o[3]));
@@ -1695,7 +1703,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) ssm_chunk_out_tc_kernel(const 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(taddr) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(taddr) : "memory");
 }
 
 // Chunked prefill, the pass between the chunk passes: carry the state across a
