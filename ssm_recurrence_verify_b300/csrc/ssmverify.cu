@@ -1272,11 +1272,6 @@ struct TCLay {
     static constexpr int kBytes = kDt + 128 * 4;
 };
 
-// MN-major layout (token s, index i): 8 (token) x 16-byte core matrices, index-contiguous.
-__device__ __forceinline__ uint32_t tc_operand_off(int s, int i) {
-    return (uint32_t)((i >> 3) * 128 + (s >> 3) * 2048 + (s & 7) * 16 + (i & 7) * 2);
-}
-
 // K-major operand: row r (M or N index), token (K index) k.
 __device__ __forceinline__ uint32_t tck_off(int r, int k) {
     return (uint32_t)((r >> 3) * 2048 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
