@@ -1730,11 +1730,32 @@ __device__ __forceinline__ float4 fma4(float l, float4 h, float4 s) {
     return make_float4(fmaf(l, h.x, s.x), fmaf(l, h.y, s.y), fmaf(l, h.z, s.z), fmaf(l, h.w, s.w));
 }
 
-__global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(kScanThreads, 4) ssm_chunk_scan_kernel(const ScanArgs a) {
     extern __shared__ float lam[];  // [nch]
     const int b = blockIdx.z, h = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float Ah = __ldg(a.A + h);
+    int sidx = b;
+    bool ok = true;
+    if (a.slot != nullptr) {
+        sidx = __ldg(a.slot + b);
+        ok = sidx >= 0 && sidx < a.nslots;
+    }
+    // this thread's vector of the cached state and of the first chunks' states: loads issued before the
+    // chunk decays are formed, so their latencies overlap
+    const long long e = ((long long)blockIdx.x * kScanThreads + tid) * kScanPerThread;  // P * N % 4 == 0
+    const bool live = e < a.PN;
+    const long long cstride = (long long)a.H * a.PN / kScanPerThread;  // chunk to chunk, in vectors
+    float4 *cache = ok && live ? reinterpret_cast<float4 *>(a.pool + ((long long)sidx * a.H + h) * a.PN + e) : nullptr;
+    float4 *w = live ? reinterpret_cast<float4 *>(a.ws + ((long long)b * a.nch * a.H + h) * a.PN + e) : nullptr;
+    float4 H = make_float4(0.f, 0.f, 0.f, 0.f);  // an invalid slot starts from h = 0
+    float4 S[kScanAhead];
+    if (live) {
+        if (cache != nullptr) H = *cache;
+#pragma unroll
+        for (int k = 0; k < kScanAhead; ++k)
+            if (k < a.nch) S[k] = __ldcs(w + k * cstride);
+    }
     // lambda_c: one warp per chunk, a fixed product tree over the chunk's tokens
     for (int c = warp; c < a.nch; c += kScanThreads / 32) {
         float prod = 1.f;
@@ -1748,28 +1769,18 @@ __global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const Scan
         for (int off = 16; off > 0; off >>= 1) prod = __fmul_rn(prod, __shfl_xor_sync(~0u, prod, off));
         if (lane == 0) lam[c] = prod;
     }
-    int sidx = b;
-    bool ok = true;
-    if (a.slot != nullptr) {
-        sidx = __ldg(a.slot + b);
-        ok = sidx >= 0 && sidx < a.nslots;
-    }
     if (!ok && blockIdx.x == 0 && h == 0 && tid == 0 && a.dev_status != nullptr)
         atomicOr(a.dev_status, SSM_STATUS_BAD_SLOT);
     if (a.vslot != nullptr && blockIdx.x == 0 && h == 0)
         for (int c = tid; c < a.nch; c += kScanThreads) a.vslot[b * a.nch + c] = ok ? b * a.nch + c : -1;
     __syncthreads();
-    const long long e = ((long long)blockIdx.x * kScanThreads + tid) * kScanPerThread;  // P * N % 4 == 0
-    if (e >= a.PN) return;
-    float4 *cache = ok ? reinterpret_cast<float4 *>(a.pool + ((long long)sidx * a.H + h) * a.PN + e) : nullptr;
-    float4 H = ok ? *cache : make_float4(0.f, 0.f, 0.f, 0.f);  // an invalid slot starts from h = 0
-    const long long cstride = (long long)a.H * a.PN / kScanPerThread;  // chunk to chunk, in vectors
-    float4 *w = reinterpret_cast<float4 *>(a.ws + ((long long)b * a.nch * a.H + h) * a.PN + e);
+    if (!live) return;
     for (int c0 = 0; c0 < a.nch; c0 += kScanAhead) {
-        float4 S[kScanAhead];
+        if (c0 > 0) {
 #pragma unroll
-        for (int k = 0; k < kScanAhead; ++k)
-            if (c0 + k < a.nch) S[k] = __ldcs(w + (c0 + k) * cstride);
+            for (int k = 0; k < kScanAhead; ++k)
+                if (c0 + k < a.nch) S[k] = __ldcs(w + (c0 + k) * cstride);
+        }
 #pragma unroll
         for (int k = 0; k < kScanAhead; ++k) {
             if (c0 + k < a.nch) {
@@ -1778,7 +1789,7 @@ __global__ void __launch_bounds__(kScanThreads) ssm_chunk_scan_kernel(const Scan
             }
         }
     }
-    if (ok) *cache = H;
+    if (cache != nullptr) *cache = H;
 }
 
 // Fixed device scratch of ssm_prefill_scratch: the chunked prefill's
