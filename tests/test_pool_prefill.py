@@ -263,3 +263,29 @@ def test_pool_layer_stack_equals_per_layer_pool_calls(cuda_device, dtype):
                 assert torch.equal(y[l][torch.tensor([0, 1, 3])], outs[l][0][torch.tensor([0, 1, 3])]), (fn, l)
         untouched = [i for i in range(nslots) if i not in (5, 0, 2)]
         assert torch.equal(stacked[:, untouched], pool0[:, untouched]), fn
+
+
+def test_prefill_tensor_memory_bad_slot(cuda_device):
+    """The tcgen05 prefill passes with one sequence on an invalid slot: its y
+    stays unwritten, the status bit is set, the valid sequence matches the
+    oracle and no other slot changes."""
+    dev = cuda_device
+    batch, H, P, N, G, T = 2, 16, 256, 128, 4, 1024
+    wl, p, t = _inputs(batch, H, P, N, G, T, synth.BF16, seed=463)
+    td = _dev(t, dev)
+    A, D = p["A"].to(dev), p["D"].to(dev)
+    nslots = 3
+    pool0 = torch.zeros(nslots, H, P, N)
+    pool0[2] = p["state0"][0]
+    pool = pool0.to(dev)
+    slot = torch.tensor([2, 7], dtype=torch.int32, device=dev)  # sequence 1: out of range
+    y = torch.full((batch, T, H, P), 7.0, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ssm.prefill(pool, slot, td["x"], td["B"], td["C"], td["dt"], A, D, y=y, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & sv.SSM_STATUS_BAD_SLOT
+    assert (y[1] == 7.0).all()
+    assert torch.equal(pool[:2].cpu(), pool0[:2])
+    ref = oracle.verify_commit(p["state0"][:1], t["x"][:1], t["B"][:1], t["C"][:1], t["dt"][:1], p["A"], p["D"], None)
+    assert rel_err(np64(y[:1]), ref["y"]) <= y_tol(torch.bfloat16)
+    assert rel_err(np64(pool[2:3]), ref["state"]) <= RTOL_STATE
