@@ -1262,6 +1262,7 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
 constexpr int kTCRows = 128;
 constexpr int kTCParts = 2;
 constexpr int kTCThreads = 256;
+constexpr int kStagePitch = 132;  // floats per row of a 128 x 128 fp32 tile staged in shared memory (padded)
 struct TCLay {
     static constexpr int kPart = 128 * 128 * 2;       // one bf16 operand: 128 rows x 128 tokens
     static constexpr int kA = 0;                      // w o U parts a1, a2
@@ -1424,8 +1425,10 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
         if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
         mbar_wait_bounded(&bar, 0u);
     } else {
+        // the accumulator through shared memory (over the operands, which the products no longer read), so
+        // that each warp then writes whole 512-byte rows
         const int r = (warp & 3) * 32 + lane, ch = (warp >> 2) * 64;
-        float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0 + r) * 128;
+        float *stage = sm<float>(0);  // [128][kStagePitch]
         const uint32_t trow = taddr + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll 1
         for (int c0 = ch; c0 < ch + 64; c0 += 16) {
@@ -1433,7 +1436,15 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
             tc_ld16(trow + c0, f);
 #pragma unroll
             for (int k = 0; k < 16; k += 4)
-                *reinterpret_cast<float4 *>(out + c0 + k) = make_float4(f[k], f[k + 1], f[k + 2], f[k + 3]);
+                *reinterpret_cast<float4 *>(stage + r * kStagePitch + c0 + k) = make_float4(f[k], f[k + 1], f[k + 2], f[k + 3]);
+        }
+        __syncthreads();
+        float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0) * 128;
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+            const int idx = it * kTCThreads + tid, row = idx >> 5, c4 = (idx & 31) * 4;
+            *reinterpret_cast<float4 *>(out + (long long)row * 128 + c4) =
+                *reinterpret_cast<const float4 *>(stage + row * kStagePitch + c4);
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1672,9 +1683,10 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
             if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
             mbar_wait_bounded(&bar, 0u);
         } else if (write_y) {
-            // y = w_t Yi + Yc + D x, this thread's half of row t
+            // y = w_t Yi + Yc + D x, this thread's half of row t, staged through shared memory (over the
+            // operands, which the products no longer read) so that each warp writes whole 512-byte rows
             const float wt = expf(__fmul_rn(Ah, cst));
-            float *yrow = a.y + ((v * 128 + t) * a.H + h) * (long long)a.P + row0;
+            float *stage = sm<float>(0);  // [128][kStagePitch]
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int c0 = ch + cc * 16;
@@ -1690,8 +1702,15 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
                         const float xv = __uint_as_float(u16_at(xd[idx >> 3], idx & 7) << 16);
                         o[e] = __fmaf_rn(wt, yi[k + e], yc[k + e]) + __fmul_rn(Dh, xv);
                     }
-                    __stcs(reinterpret_cast<float4 *>(yrow + c0 + k), make_float4(o[0], o[1], o[2], o[3]));
+                    *reinterpret_cast<float4 *>(stage + t * kStagePitch + c0 + k) = make_float4(o[0], o[1], o[2], o[3]);
                 }
+            }
+            __syncthreads();  // write_y is the same for the whole CTA
+#pragma unroll 4
+            for (int it = 0; it < 16; ++it) {
+                const int idx = it * kOutThreads + tid, row = idx >> 5, c4 = (idx & 31) * 4;
+                __stcs(reinterpret_cast<float4 *>(a.y + ((v * 128 + row) * a.H + h) * (long long)a.P + row0 + c4),
+                       *reinterpret_cast<const float4 *>(stage + row * kStagePitch + c4));
             }
         }
     }
