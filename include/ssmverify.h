@@ -256,10 +256,12 @@ int ssm_prefill(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, c
 /*
  * ssm_prefill_scratch -- ssm_prefill without a caller workspace: the chunked
  * form runs in a fixed device array of SSM_PREFILL_SCRATCH_BYTES inside the
- * library (allocated with the library's device code, once per device).
- * Shapes whose chunked workspace (ssm_prefill_workspace_bytes) exceeds it are
- * rejected with SSM_ERR_SHAPE before anything is launched; nothing in the
- * array needs to start at zero. Calls that may overlap in time (other
+ * library (allocated with the library's device code, once per device). The
+ * chunk length is chosen among those whose workspace fits in the array;
+ * where none fits the one-pass form runs (it needs no workspace, but takes
+ * the prompt token after token), so results equal ssm_prefill's with a
+ * workspace of SSM_PREFILL_SCRATCH_BYTES. Nothing in the array needs to start
+ * at zero. Calls that may overlap in time (other
  * streams, other host threads, other processes sharing the context) race on
  * the array: issue them one after another. The pages have no counterpart;
  * this exists for callers that cannot allocate device memory.

@@ -2099,13 +2099,19 @@ int64_t prefill_ws_bytes(const ssm_desc_t *d, int L) {
     return prefill_ws_states(d, L) + ((int64_t)d->batch * (d->ntok / L) * 4 + 15) / 16 * 16;
 }
 
-// Chunk length of a chunked prefill: the largest of 128, 64, 32, 16
-// that divides the prompt into at least two chunks, fits the workspace and
-// gives one wave of tiles (four per SM); the smallest fitting one if none
-// reaches a wave. 0: the one-pass form (it fills the device by itself, or no
-// chunk length fits).
+// Chunk length of a chunked prefill: 128 for the shapes of the tensor-memory
+// chunk passes when the workspace holds it; otherwise the largest of 128,
+// 64, 32, 16 that divides the prompt into at least two chunks, fits the
+// workspace and gives one wave of tiles (four per SM), the smallest fitting
+// one if none reaches a wave. 0: the one-pass form (it fills the device by
+// itself, or no chunk length fits).
 int prefill_chunk_len(const ssm_desc_t *d, int64_t ws_bytes) {
     const int T = d->ntok;
+    // shapes the tensor-memory chunk passes take: 128-token chunks whenever the workspace allows, since
+    // those passes cost far less per token than the recurrence, whatever the grid
+    if (d->in_dtype == SSM_BF16 && d->dstate == 128 && d->headdim % 128 == 0 && T % 128 == 0 && T / 128 >= 2 &&
+        T / 128 <= kMaxChunks && (ws_bytes < 0 || prefill_ws_bytes(d, 128) <= ws_bytes))
+        return 128;
     const int ROWS = rows_per_tile(d->dstate);
     const int64_t ptiles = (d->headdim + ROWS - 1) / ROWS;
     const int64_t base = (int64_t)d->batch * d->nheads * ptiles;
@@ -2513,8 +2519,9 @@ int ssm_prefill_scratch(const ssm_desc_t *desc, const ssm_pool_t *pool, const vo
     if (desc->nlayers > 1) return SSM_ERR_UNSUPPORTED;
     if (pool == nullptr) return SSM_ERR_NULL;
     if (desc->batch == 0) return SSM_OK;
-    const int64_t need = ssm_prefill_workspace_bytes(desc);
-    if (need > SSM_PREFILL_SCRATCH_BYTES) return SSM_ERR_SHAPE;  // more than the fixed scratch holds
+    // the chunk length the fixed scratch holds (0: the one-pass form, which needs no workspace)
+    const int L = prefill_chunk_len(desc, SSM_PREFILL_SCRATCH_BYTES);
+    const int64_t need = L > 0 ? prefill_ws_bytes(desc, L) : 0;
     void *ws = nullptr;
     if (need > 0) {
         cudaError_t e = cudaSuccess;
