@@ -367,6 +367,26 @@ int ssm_accept_sample(const ssm_accept_desc_t *desc, const void *target_logits, 
  */
 int ssm_copy_from_host(void *dst, const void *src, int64_t bytes, void *stream);
 
+/*
+ * ssm_copy_from_host_n -- several such copies in one launch: segment i copies
+ * segs[i].bytes from page-locked host memory segs[i].src to device memory
+ * segs[i].dst. A step's inputs (x, B, C, dt, accept_len of a sequence chunk)
+ * then cost one launch instead of one per tensor. `segs` is a host array of
+ * 0 <= nseg <= SSM_COPY_MAX_SEGMENTS entries, read before the call returns.
+ * Per segment the rules of ssm_copy_from_host apply; in addition no two
+ * segments' destinations, and no destination and source, may overlap
+ * (SSM_ERR_ALIAS). Where every segment's source and destination are 16-byte
+ * aligned a single kernel copies them all; otherwise each segment takes its
+ * own ssm_copy_from_host.
+ */
+#define SSM_COPY_MAX_SEGMENTS 8
+typedef struct {
+    void *dst;        /* device memory */
+    const void *src;  /* page-locked host memory */
+    int64_t bytes;    /* >= 0 */
+} ssm_copy_segment_t;
+int ssm_copy_from_host_n(const ssm_copy_segment_t *segs, int32_t nseg, void *stream);
+
 /* A static, human-readable string for an SSM_* return code. */
 const char *ssm_strerror(int code);
 

@@ -90,10 +90,14 @@ class HostPipeline:
             with torch.cuda.stream(self.s_in):
                 if self.freed[k] is not None:
                     self.s_in.wait_event(self.freed[k])
-                for dst, src in ((self.slot_x[k][:n], x[lo:hi]), (self.slot_B[k][:n], B[lo:hi]),
-                                 (self.slot_C[k][:n], C[lo:hi]), (self.slot_dt[k][:n], dt[lo:hi]),
-                                 (self.slot_acc[k][:n], accept_len[lo:hi])):
-                    self._h2d(dst, src)
+                pairs = ((self.slot_x[k][:n], x[lo:hi]), (self.slot_B[k][:n], B[lo:hi]),
+                         (self.slot_C[k][:n], C[lo:hi]), (self.slot_dt[k][:n], dt[lo:hi]),
+                         (self.slot_acc[k][:n], accept_len[lo:hi]))
+                if all(src.is_pinned() and src.is_contiguous() for _, src in pairs):
+                    sv.copy_from_host_n(pairs, stream=self.s_in)  # the chunk's inputs in one launch
+                else:
+                    for dst, src in pairs:
+                        self._h2d(dst, src)
                 arrived = torch.cuda.Event()
                 arrived.record(self.s_in)
             with torch.cuda.stream(self.s_k):

@@ -40,7 +40,9 @@ SSM_PREFILL_SCRATCH_BYTES = 64 << 20
 EXPORTS = ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
            "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool", "ssm_step_pool",
            "ssm_prefill", "ssm_prefill_workspace_bytes", "ssm_prefill_scratch", "ssm_selftest_wait_timeout", "ssm_accept_greedy",
-           "ssm_accept_sample", "ssm_copy_from_host", "ssm_strerror", "ssm_last_cuda_error", "ssm_version")
+           "ssm_accept_sample", "ssm_copy_from_host", "ssm_copy_from_host_n", "ssm_strerror", "ssm_last_cuda_error",
+           "ssm_version")
+SSM_COPY_MAX_SEGMENTS = 8
 
 
 class SsmDesc(ctypes.Structure):
@@ -52,6 +54,10 @@ class SsmDesc(ctypes.Structure):
 class PoolDesc(ctypes.Structure):
     _fields_ = [("states", ctypes.c_void_p), ("slot", ctypes.c_void_p), ("nslots", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class CopySegment(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_int64)]
 
 
 class AcceptDesc(ctypes.Structure):
@@ -97,12 +103,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_prefill.argtypes = [dp, pp] + [vp] * 8 + [ctypes.c_int64, vp, vp]
     lib.ssm_prefill_scratch.argtypes = [dp, pp] + [vp] * 9
     lib.ssm_copy_from_host.argtypes = [vp, vp, ctypes.c_int64, vp]
+    lib.ssm_copy_from_host_n.argtypes = [ctypes.POINTER(CopySegment), ctypes.c_int32, vp]
     lib.ssm_prefill_workspace_bytes.argtypes = [dp]
     lib.ssm_prefill_workspace_bytes.restype = ctypes.c_int64
     for f in ("ssm_verify", "ssm_commit", "ssm_verify_commit", "ssm_commit_verify", "ssm_step",
               "ssm_verify_pool", "ssm_commit_pool", "ssm_verify_commit_pool", "ssm_commit_verify_pool",
               "ssm_step_pool", "ssm_prefill", "ssm_prefill_scratch", "ssm_selftest_wait_timeout", "ssm_accept_greedy", "ssm_accept_sample",
-              "ssm_copy_from_host", "ssm_last_cuda_error", "ssm_version"):
+              "ssm_copy_from_host", "ssm_copy_from_host_n", "ssm_last_cuda_error", "ssm_version"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ssm_strerror.argtypes = [ctypes.c_int]
     lib.ssm_strerror.restype = ctypes.c_char_p
@@ -470,3 +477,24 @@ def copy_from_host(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.T
     _check(load_library().ssm_copy_from_host(_ptr(dst), _ptr(src), dst.numel() * dst.element_size(),
                                              _stream(stream)))
     return dst
+
+
+def copy_from_host_n(pairs, stream=None) -> None:
+    """Several copies from page-locked host tensors to CUDA tensors of the same
+    size, ``pairs`` = [(dst, src), ...] (at most SSM_COPY_MAX_SEGMENTS), in
+    one launch (asynchronous on the stream)."""
+    if len(pairs) > SSM_COPY_MAX_SEGMENTS:
+        raise ValueError(f"at most {SSM_COPY_MAX_SEGMENTS} segments")
+    segs = (CopySegment * max(1, len(pairs)))()
+    for i, (dst, src) in enumerate(pairs):
+        if dst.numel() * dst.element_size() != src.numel() * src.element_size():
+            raise ValueError("dst and src must have the same number of bytes")
+        if dst.numel() == 0:  # nothing to copy (an empty tensor reports no page-locked storage)
+            segs[i] = CopySegment(None, None, 0)
+            continue
+        if not dst.is_cuda or src.is_cuda or not src.is_pinned():
+            raise ValueError("dst must be a CUDA tensor and src a page-locked (pinned) host tensor")
+        if not dst.is_contiguous() or not src.is_contiguous():
+            raise ValueError("dst and src must be contiguous")
+        segs[i] = CopySegment(dst.data_ptr(), src.data_ptr(), dst.numel() * dst.element_size())
+    _check(load_library().ssm_copy_from_host_n(segs, len(pairs), _stream(stream)))

@@ -397,3 +397,21 @@ def test_pool_and_prefill_validation(lib):
     assert lib.ssm_prefill(ctypes.byref(d0), ctypes.byref(pool(None)), *([None] * 8), 0, None, None) == sv.SSM_OK
     assert lib.ssm_prefill_workspace_bytes(ctypes.byref(d0)) == 0
     assert lib.ssm_prefill_scratch(ctypes.byref(d), None, *([None] * 9)) == sv.SSM_ERR_NULL
+
+
+@no_gpu_only
+def test_copy_from_host_n_validation(lib):
+    """Segment count, null pointers, negative sizes and overlapping
+    destinations are refused before anything else is looked at."""
+    Seg = sv.CopySegment
+    mk = lambda *t: (Seg * max(1, len(t)))(*t)
+    a, b = BASE, BASE + (1 << 30)
+    assert lib.ssm_copy_from_host_n(mk(), 0, None) == sv.SSM_OK
+    assert lib.ssm_copy_from_host_n(mk(), -1, None) == sv.SSM_ERR_SHAPE
+    assert lib.ssm_copy_from_host_n((Seg * 9)(), 9, None) == sv.SSM_ERR_SHAPE
+    assert lib.ssm_copy_from_host_n(None, 1, None) == sv.SSM_ERR_NULL
+    assert lib.ssm_copy_from_host_n(mk(Seg(a, b, -1)), 1, None) == sv.SSM_ERR_SHAPE
+    assert lib.ssm_copy_from_host_n(mk(Seg(None, b, 16)), 1, None) == sv.SSM_ERR_NULL
+    assert lib.ssm_copy_from_host_n(mk(Seg(a, b, 64), Seg(a + 32, b + 4096, 64)), 2, None) == sv.SSM_ERR_ALIAS
+    assert lib.ssm_copy_from_host_n(mk(Seg(a, b, 64), Seg(b + 32, a + 4096, 64)), 2, None) == sv.SSM_ERR_ALIAS
+    assert lib.ssm_copy_from_host_n(mk(Seg(a, b, 0), Seg(a, b, 0)), 2, None) == sv.SSM_OK  # empty: nothing to do

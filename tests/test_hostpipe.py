@@ -96,3 +96,20 @@ def test_copy_from_host_refuses_pageable_memory(cuda_device):
     import ctypes
     rc = lib.ssm_copy_from_host(ctypes.c_void_p(d.data_ptr()), ctypes.c_void_p(h.data_ptr()), 64, None)
     assert rc == sv.SSM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("offset", [0, 3])
+def test_copy_from_host_n(cuda_device, offset):
+    """Several copies in one call: segments of 5 MB, 16 KB + 9 bytes, 0 bytes,
+    7 bytes and 4 KB are exact (offset 0: one kernel over all segments;
+    offset 3: unaligned, each segment on its own); bytes around them stay."""
+    from ssm_recurrence_verify_b300 import ssmverify as sv
+    sizes = [5 << 20, (16 << 10) + 9, 0, 7, 4096]
+    g = torch.Generator().manual_seed(11)
+    hs = [torch.randint(0, 256, (n + offset,), dtype=torch.uint8, generator=g).pin_memory() for n in sizes]
+    ds = [torch.full((n + offset + 16,), 7, dtype=torch.uint8, device=cuda_device) for n in sizes]
+    sv.copy_from_host_n([(d[offset:offset + n], h[offset:]) for d, h, n in zip(ds, hs, sizes)])
+    torch.cuda.synchronize()
+    for d, h, n in zip(ds, hs, sizes):
+        assert torch.equal(d[offset:offset + n].cpu(), h[offset:])
+        assert (d[:offset] == 7).all() and (d[offset + n:] == 7).all()
