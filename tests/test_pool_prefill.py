@@ -289,3 +289,10 @@ def test_prefill_tensor_memory_bad_slot(cuda_device):
     ref = oracle.verify_commit(p["state0"][:1], t["x"][:1], t["B"][:1], t["C"][:1], t["dt"][:1], p["A"], p["D"], None)
     assert rel_err(np64(y[:1]), ref["y"]) <= y_tol(torch.bfloat16)
     assert rel_err(np64(pool[2:3]), ref["state"]) <= RTOL_STATE
+
+
+@pytest.mark.parametrize("T", [256, 384])
+def test_prefill_tensor_memory_few_chunks(cuda_device, T):
+    """The tcgen05 passes with two and three 128-token chunks (bf16, N = 128,
+    P = 128) on a small batch, against the oracle."""
+    _prefill_case(cuda_device, 3, 4, 128, 128, 2, T, synth.BF16, seed=470 + T)
