@@ -41,9 +41,11 @@
  * resident blocks per SM, per kernel and device), so calls are thread-safe
  * (ssm_prefill_scratch alone also uses a fixed device array; see there).
  * Every entry point only validates its arguments and enqueues one kernel
- * (ssm_prefill: up to three) on `stream` (a cudaStream_t passed as void*,
- * NULL = the legacy default stream) on the current device. Calls are
- * asynchronous. ssm_copy_from_host alone takes a host pointer (its source).
+ * (ssm_prefill: up to three; ssm_copy_from_host_n: one per segment when the
+ * segments are not all 16-byte aligned) on `stream` (a cudaStream_t passed
+ * as void*, NULL = the legacy default stream) on the current device. Calls
+ * are asynchronous. ssm_copy_from_host and ssm_copy_from_host_n alone take
+ * host pointers (their sources).
  *
  * Errors: the return value is SSM_OK or an SSM_ERR_* code. Argument errors
  * are detected on the host before anything is launched (no device work is
