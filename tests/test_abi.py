@@ -415,3 +415,11 @@ def test_copy_from_host_n_validation(lib):
     assert lib.ssm_copy_from_host_n(mk(Seg(a, b, 64), Seg(a + 32, b + 4096, 64)), 2, None) == sv.SSM_ERR_ALIAS
     assert lib.ssm_copy_from_host_n(mk(Seg(a, b, 64), Seg(b + 32, a + 4096, 64)), 2, None) == sv.SSM_ERR_ALIAS
     assert lib.ssm_copy_from_host_n(mk(Seg(a, b, 0), Seg(a, b, 0)), 2, None) == sv.SSM_OK  # empty: nothing to do
+
+
+def test_copy_from_host_n_binding_limits():
+    """The binding refuses more segments than the library takes, before any
+    device or pointer is looked at."""
+    pairs = [(torch.zeros(4), torch.zeros(4))] * (sv.SSM_COPY_MAX_SEGMENTS + 1)
+    with pytest.raises(ValueError):
+        sv.copy_from_host_n(pairs)

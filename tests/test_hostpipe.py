@@ -113,3 +113,20 @@ def test_copy_from_host_n(cuda_device, offset):
     for d, h, n in zip(ds, hs, sizes):
         assert torch.equal(d[offset:offset + n].cpu(), h[offset:])
         assert (d[:offset] == 7).all() and (d[offset + n:] == 7).all()
+
+
+def test_copy_from_host_n_refuses_pageable_memory(cuda_device):
+    """One pageable source among page-locked ones: the call is refused before
+    anything is copied (the binding raises; the C entry returns UNSUPPORTED)."""
+    from ssm_recurrence_verify_b300 import ssmverify as sv
+    good = torch.arange(64, dtype=torch.uint8).pin_memory()
+    bad = torch.zeros(64, dtype=torch.uint8)  # not page-locked
+    d1 = torch.full((64,), 7, dtype=torch.uint8, device=cuda_device)
+    d2 = torch.full((64,), 7, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(ValueError):
+        sv.copy_from_host_n([(d1, good), (d2, bad)])
+    segs = (sv.CopySegment * 2)(sv.CopySegment(d1.data_ptr(), good.data_ptr(), 64),
+                                sv.CopySegment(d2.data_ptr(), bad.data_ptr(), 64))
+    assert sv.load_library().ssm_copy_from_host_n(segs, 2, None) == sv.SSM_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (d1 == 7).all() and (d2 == 7).all()
