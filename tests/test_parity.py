@@ -283,14 +283,15 @@ def _stack(ds, keys):
     return {k: torch.stack([d[k] for d in ds]) for k in keys}
 
 
-@pytest.mark.parametrize("K,dtype", [(8, synth.BF16), (12, synth.F32)])
-def test_layer_stack_equals_per_layer_calls(cuda_device, K, dtype):
+@pytest.mark.parametrize("K,dtype,P,N", [(8, synth.BF16, 64, 128), (12, synth.F32, 64, 128), (6, synth.F32, 40, 256)])
+def test_layer_stack_equals_per_layer_calls(cuda_device, K, dtype, P, N):
     """nlayers = L: one call over [L]-leading slabs (A, D [L][H]; accept_len
     [batch] shared) gives, bit for bit, the L single-layer calls on the
-    slices, in every entry point."""
+    slices, in every entry point (also N = 256, two warps per band, with a
+    ragged last tile)."""
     dev = cuda_device
     L, batch = 3, 5
-    wl = synth.custom_workload(batch, 4, 64, 128, 2, K, dtype, seed=880 + K)
+    wl = synth.custom_workload(batch, 4, P, N, 2, K, dtype, seed=880 + K)
     ds = [synth.draw_layer_round(wl, rnd=0, layer=l) for l in range(L)]
     acc = ds[0]["accept_len"].to(dev)
     S = {k: v.to(dev) for k, v in _stack(ds, ("state0", "x", "B", "C", "dt", "A", "D")).items()}
