@@ -1459,7 +1459,9 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
 // recurrence,
 //     y_t = w_t (C_t . H0) + sum_{s<=t} exp(A (cs_t - cs_s)) dt_s (C_t . B_s) x_s + D x_t,
 //     cs_t = sum_{r<=t} dt_r,   w_t = exp(A cs_t),
-// for 128 rows p of one head. Three products accumulate in tensor memory:
+// for 128 rows p of one head (or 64: the tile's rows PR, where P is a multiple
+// of 64 but not of 128, with Yi and Yc then N = 64 products). Three products
+// accumulate in tensor memory:
 //   Yi = C H0^T   (128 tokens x 128 rows, over 128 state channels; H0 split
 //                  into two bf16 parts, C exact),
 //   G  = C B^T    (128 x 128 tokens; bf16, exact inputs),
@@ -1497,7 +1499,10 @@ struct OutLay {
     static constexpr int kBytes = kDt + 512;
 };
 
+template <int PR>  // rows of the tile: 128, or 64 (the products over rows are then N = 64)
 __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const OutArgs a) {
+    static_assert(PR == 128 || PR == 64, "tile rows");
+    constexpr uint32_t kIdescRows = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(PR >> 3) << 17) | ((128u >> 4) << 24);
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t tmem_base;
     __shared__ float wsum[4];
@@ -1510,7 +1515,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
     const int h = (int)(vh % a.H);
     const long long v = vh / a.H;
     const int gi = h / (a.H / a.G);
-    const int row0 = ptile * 128;
+    const int row0 = ptile * PR;
     const float Ah = __ldg(a.A + h), Dh = __ldg(a.D + h);
     const bool write_y = a.vslot == nullptr || __ldg(a.vslot + v) >= 0;
     const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(a.x);
@@ -1520,6 +1525,10 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
     // warp task (8 consecutive rows x 4 consecutive 16-byte chunks), 8 per warp: conflict-free stores
     auto task_r = [&](int it) { return ((warp + 8 * it) & 15) * 8 + (lane & 7); };
     auto task_q = [&](int it) { return ((warp + 8 * it) >> 4) * 4 + (lane >> 3); };
+    // the same over the tile's PR rows (PR / 16 tasks per warp)
+    constexpr int kRG = PR / 8;
+    auto htask_r = [&](int it) { return ((warp + 8 * it) % kRG) * 8 + (lane & 7); };
+    auto htask_q = [&](int it) { return ((warp + 8 * it) / kRG) * 4 + (lane >> 3); };
 
     // C and B (K-major, row = token): straight into their operand layouts
 #pragma unroll 4
@@ -1531,10 +1540,10 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
     }
     // H0 (row p, K-major): high part into its operand now, low part kept packed for the second product
     const float *H0 = a.ws + ((v * a.H + h) * (long long)a.P + row0) * 128;
-    uint4 hlo[8];
+    uint4 hlo[PR / 16];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const float *src = H0 + task_r(it) * 128 + task_q(it) * 8;
+    for (int it = 0; it < PR / 16; ++it) {
+        const float *src = H0 + htask_r(it) * 128 + htask_q(it) * 8;
         const float4 f0 = __ldcs(reinterpret_cast<const float4 *>(src));
         const float4 f1 = __ldcs(reinterpret_cast<const float4 *>(src + 4));
         const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
@@ -1545,7 +1554,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
             hi[e / 2] = bf16_bits(a0) | (bf16_bits(a1) << 16);
             lo[e / 2] = pack_bf16x2(f[e] - __bfloat162float(a0), f[e + 1] - __bfloat162float(a1));
         }
-        *reinterpret_cast<uint4 *>(sb + OutLay::kP2 + tck_off(task_r(it), task_q(it) * 8)) =
+        *reinterpret_cast<uint4 *>(sb + OutLay::kP2 + tck_off(htask_r(it), htask_q(it) * 8)) =
             make_uint4(hi[0], hi[1], hi[2], hi[3]);
         hlo[it] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -1590,29 +1599,35 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
                      kTCIdescKK, kk > 0 ? 1u : 0u);
         for (int kk = 0; kk < 8; ++kk)  // Yi = C H0^T, high part
             tc_mma_i(taddr, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP2 + kk * 256),
-                     kTCIdescKK, kk > 0 ? 1u : 0u);
+                     kIdescRows, kk > 0 ? 1u : 0u);
         tc_commit(&bar);
     }
     // this thread's 8 x 8 block of x (tokens s0 .. s0+7, rows p0 .. p0+7), loaded while the products run
-    const int bp = tid & 15, bs = tid >> 4, p0 = bp * 8, s0 = bs * 8;
+    // (PR / 8 row blocks x 16 token blocks: threads past them hold none)
+    constexpr int kPB = PR / 8;
+    const bool hasx = tid < kPB * 16;
+    const int bp = tid % kPB, bs = tid / kPB, p0 = bp * 8, s0 = bs * 8;
     uint4 xr[8];
+    if (hasx) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        xr[i] = __ldg(reinterpret_cast<const uint4 *>(xg + ((v * 128 + s0 + i) * a.H + h) * (long long)a.P + row0 + p0));
+        for (int i = 0; i < 8; ++i)
+            xr[i] = __ldg(reinterpret_cast<const uint4 *>(xg + ((v * 128 + s0 + i) * a.H + h) * (long long)a.P + row0 +
+                                                          p0));
+    }
     bool ok = mbar_wait_bounded(&bar, 0u);
     int phase = 1;
     if (!__syncthreads_or(!ok)) {
         // B is no longer read: the low part of H0 takes its place; Yi += C H0^T, low part
 #pragma unroll
-        for (int it = 0; it < 8; ++it)
-            *reinterpret_cast<uint4 *>(sb + OutLay::kP1 + tck_off(task_r(it), task_q(it) * 8)) = hlo[it];
+        for (int it = 0; it < PR / 16; ++it)
+            *reinterpret_cast<uint4 *>(sb + OutLay::kP1 + tck_off(htask_r(it), htask_q(it) * 8)) = hlo[it];
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             for (int kk = 0; kk < 8; ++kk)
                 tc_mma_i(taddr, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
-                         kTCIdescKK, 1u);
+                         kIdescRows, 1u);
             tc_commit(&bar);
         }
         ok = mbar_wait_bounded(&bar, 1u);
@@ -1620,7 +1635,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const int t = (warp & 3) * 32 + lane;  // this thread's token (tensor-memory lane)
-    const int ch = (warp >> 2) * 64;       // its half of the columns
+    const int ch = (warp >> 2) * 64;       // its half of the 128 G columns (and of the PR y columns: ch * PR / 128)
     const uint32_t trow = taddr + ((uint32_t)((warp & 3) * 32) << 16);
     if (__syncthreads_or(!ok)) {
         if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, SSM_STATUS_TIMEOUT);
@@ -1651,13 +1666,15 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
             *reinterpret_cast<uint4 *>(sb + OutLay::kP0 + tck_off(t, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             *reinterpret_cast<uint4 *>(sb + OutLay::kP0 + tck_off(t, c + 8)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
         }
+        if (hasx) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int j = (k + lane) & 7;  // row p0 + j: element j of each token row; rotated per lane
-            uint32_t w[4];
+            for (int k = 0; k < 8; ++k) {
+                const int j = (k + lane) & 7;  // row p0 + j: element j of each token row; rotated per lane
+                uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) w[e / 2] = u16_at(xr[e], j) | (u16_at(xr[e + 1], j) << 16);
-            *reinterpret_cast<uint4 *>(sb + OutLay::kP1 + tck_off(p0 + j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 8; e += 2) w[e / 2] = u16_at(xr[e], j) | (u16_at(xr[e + 1], j) << 16);
+                *reinterpret_cast<uint4 *>(sb + OutLay::kP1 + tck_off(p0 + j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
         fence_proxy_async_smem();
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1666,17 +1683,19 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
         if (tid == 0) {
             for (int kk = 0; kk < 8; ++kk)  // Yc = M X, both parts of M
                 tc_mma_i(taddr + 128, tck_desc(base + OutLay::kP2 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
-                         kTCIdescKK, kk > 0 ? 1u : 0u);
+                         kIdescRows, kk > 0 ? 1u : 0u);
             for (int kk = 0; kk < 8; ++kk)
                 tc_mma_i(taddr + 128, tck_desc(base + OutLay::kP0 + kk * 256), tck_desc(base + OutLay::kP1 + kk * 256),
-                         kTCIdescKK, 1u);
+                         kIdescRows, 1u);
             tc_commit(&bar);
         }
         // this thread's x values for D x (row t, its half of the columns), from L2 while the product runs
-        const __nv_bfloat16 *xrow = xg + ((v * 128 + t) * a.H + h) * (long long)a.P + row0 + ch;
-        uint4 xd[8];
+        constexpr int kHalf = PR / 2;  // y columns per thread
+        const int cy = (warp >> 2) * kHalf;
+        const __nv_bfloat16 *xrow = xg + ((v * 128 + t) * a.H + h) * (long long)a.P + row0 + cy;
+        uint4 xd[kHalf / 8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xd[i] = __ldg(reinterpret_cast<const uint4 *>(xrow + 8 * i));
+        for (int i = 0; i < kHalf / 8; ++i) xd[i] = __ldg(reinterpret_cast<const uint4 *>(xrow + 8 * i));
         ok = mbar_wait_bounded(&bar, 0u);  // third phase
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (__syncthreads_or(!ok)) {
@@ -1688,8 +1707,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
             const float wt = expf(__fmul_rn(Ah, cst));
             float *stage = sm<float>(0);  // [128][kStagePitch]
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c0 = ch + cc * 16;
+            for (int cc = 0; cc < kHalf / 16; ++cc) {
+                const int c0 = cy + cc * 16;
                 float yi[16], yc[16];
                 tc_ld16(trow + c0, yi);
                 tc_ld16(trow + 128 + c0, yc);
@@ -1707,8 +1726,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) ssm_chunk_out_tc_kernel(const 
             }
             __syncthreads();  // write_y is the same for the whole CTA
 #pragma unroll 4
-            for (int it = 0; it < 16; ++it) {
-                const int idx = it * kOutThreads + tid, row = idx >> 5, c4 = (idx & 31) * 4;
+            for (int it = 0; it < PR / 8; ++it) {  // 128 rows x PR / 4 vectors
+                const int idx = it * kOutThreads + tid, row = idx / (PR / 4), c4 = (idx % (PR / 4)) * 4;
                 __stcs(reinterpret_cast<float4 *>(a.y + ((v * 128 + row) * a.H + h) * (long long)a.P + row0 + c4),
                        *reinterpret_cast<const float4 *>(stage + row * kStagePitch + c4));
             }
@@ -2109,7 +2128,7 @@ int prefill_chunk_len(const ssm_desc_t *d, int64_t ws_bytes) {
     const int T = d->ntok;
     // shapes the tensor-memory chunk passes take: 128-token chunks whenever the workspace allows, since
     // those passes cost far less per token than the recurrence, whatever the grid
-    if (d->in_dtype == SSM_BF16 && d->dstate == 128 && d->headdim % 128 == 0 && T % 128 == 0 && T / 128 >= 2 &&
+    if (d->in_dtype == SSM_BF16 && d->dstate == 128 && d->headdim % 64 == 0 && T % 128 == 0 && T / 128 >= 2 &&
         T / 128 <= kMaxChunks && (ws_bytes < 0 || prefill_ws_bytes(d, 128) <= ws_bytes))
         return 128;
     const int ROWS = rows_per_tile(d->dstate);
@@ -2157,17 +2176,19 @@ cudaError_t launch_chunk_state_tc(const CSArgs &a, long long ntiles, cudaStream_
     return cudaGetLastError();
 }
 
+template <int PR>
 cudaError_t launch_chunk_out_tc(const OutArgs &a, long long ntiles, cudaStream_t s) {
     static std::atomic<int> ready[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices || ready[dev].load(std::memory_order_relaxed) == 0) {
-        e = cudaFuncSetAttribute(ssm_chunk_out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, OutLay::kBytes);
+        e = cudaFuncSetAttribute(ssm_chunk_out_tc_kernel<PR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 OutLay::kBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_relaxed);
     }
-    ssm_chunk_out_tc_kernel<<<(unsigned)ntiles, kOutThreads, OutLay::kBytes, s>>>(a);
+    ssm_chunk_out_tc_kernel<PR><<<(unsigned)ntiles, kOutThreads, OutLay::kBytes, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -2296,7 +2317,10 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         return SSM_ERR_CUDA;
     }
 
-    if (tc_ok && aligned(C, 16) && aligned(y, 16)) {  // the chunked output form on the tensor cores
+    // the chunked output form on the tensor cores: bf16, N = 128, 128-token chunks, 64- or 128-row tiles
+    const bool tc_out = cs_ok && d->in_dtype == SSM_BF16 && N == 128 && L == 128 && P % 64 == 0 && aligned(C, 16) &&
+                        aligned(y, 16);
+    if (tc_out) {
         OutArgs oa;
         oa.x = x; oa.B = B; oa.C = C; oa.dt = dt;
         oa.A = A; oa.D = D;
@@ -2305,9 +2329,11 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         oa.y = y;
         oa.dev_status = dev_status;
         oa.H = (int)H; oa.P = (int)P; oa.G = (int)G;
-        oa.ptiles = (int)(P / kTCRows);
-        const cudaError_t e3 = launch_chunk_out_tc(oa, (long long)dv.batch * H * (P / kTCRows),
-                                                   static_cast<cudaStream_t>(stream));
+        const int pr = P % 128 == 0 ? 128 : 64;
+        oa.ptiles = (int)(P / pr);
+        const long long nt3 = (long long)dv.batch * H * (P / pr);
+        const cudaError_t e3 = pr == 128 ? launch_chunk_out_tc<128>(oa, nt3, static_cast<cudaStream_t>(stream))
+                                         : launch_chunk_out_tc<64>(oa, nt3, static_cast<cudaStream_t>(stream));
         if (e3 != cudaSuccess) {
             g_last_cuda_error = (int)e3;
             return SSM_ERR_CUDA;

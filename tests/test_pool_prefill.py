@@ -265,12 +265,13 @@ def test_pool_layer_stack_equals_per_layer_pool_calls(cuda_device, dtype):
         assert torch.equal(stacked[:, untouched], pool0[:, untouched]), fn
 
 
-def test_prefill_tensor_memory_bad_slot(cuda_device):
-    """The tcgen05 prefill passes with one sequence on an invalid slot: its y
-    stays unwritten, the status bit is set, the valid sequence matches the
-    oracle and no other slot changes."""
+@pytest.mark.parametrize("P", [256, 64])
+def test_prefill_tensor_memory_bad_slot(cuda_device, P):
+    """The tcgen05 prefill passes (128- and 64-row output tiles) with one
+    sequence on an invalid slot: its y stays unwritten, the status bit is set,
+    the valid sequence matches the oracle and no other slot changes."""
     dev = cuda_device
-    batch, H, P, N, G, T = 2, 16, 256, 128, 4, 1024
+    batch, H, N, G, T = 2, 16, 128, 4, 1024
     wl, p, t = _inputs(batch, H, P, N, G, T, synth.BF16, seed=463)
     td = _dev(t, dev)
     A, D = p["A"].to(dev), p["D"].to(dev)
@@ -296,3 +297,11 @@ def test_prefill_tensor_memory_few_chunks(cuda_device, T):
     """The tcgen05 passes with two and three 128-token chunks (bf16, N = 128,
     P = 128) on a small batch, against the oracle."""
     _prefill_case(cuda_device, 3, 4, 128, 128, 2, T, synth.BF16, seed=470 + T)
+
+
+@pytest.mark.parametrize("P", [64, 192])
+def test_prefill_tensor_memory_64_row_tiles(cuda_device, P):
+    """The tcgen05 output pass on 64-row tiles: P a multiple of 64 but not of
+    128 (one and three tiles per head; the chunk states come from the mma.sync
+    pass), bf16, N = 128, four 128-token chunks, against the oracle."""
+    _prefill_case(cuda_device, 2, 4, P, 128, 2, 512, synth.BF16, seed=475 + P)
