@@ -1130,7 +1130,7 @@ struct CSArgs {
     const float *A;
     float *ws;               // [chunks][H][P][N]
     uint32_t *dev_status;    // nullable (the tensor-memory kernel's bounded wait)
-    int H, P, G, L, ptiles;
+    int H, P, G, L, ptiles;  // ptiles: tiles of a chunk (P / 64 per head; H P / 128 on the tensor cores)
 };
 
 template <typename Tin, int N>
@@ -1242,8 +1242,10 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
 
 // The same first pass on the 5th-generation tensor cores (tcgen05), for bf16
 // inputs, N = 128, L = 128 and 128-row tiles: one CTA computes
-// S[p][n] = sum_s (w_s u_s[p]) B_s[n] for 128 rows of one head of one chunk
-// as an M = 128, N = 128, K = 128 product accumulated in tensor memory.
+// S[p][n] = sum_s (w_s u_s[p]) B_s[n] for 128 rows of one chunk as an
+// M = 128, N = 128, K = 128 product accumulated in tensor memory. The rows
+// are 128 consecutive rows h P + p of the chunk's H P: of one head, or at
+// P = 64 of two heads of one group (B is shared, w and dt are per head).
 //  * Operands in shared memory, K-major (token index contiguous), no swizzle:
 //    8-row x 16-byte core matrices; element (row r, token s) of an operand
 //    sits at byte (r / 8) * 2048 + (s / 8) * 128 + (r % 8) * 16 + (s % 8) * 2;
@@ -1255,7 +1257,7 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
 //    16 significant bits, |a - a1 - a2| <= 2^-18 |a|); B is bf16 and exact.
 //    2 parts x 8 MMAs of K = 16 tokens (tcgen05.mma kind::f16, bf16 x bf16,
 //    fp32 accumulation), issued by one thread; tcgen05.commit signals an
-//    mbarrier, waited on with a time limit. 97.5 KB of shared memory: two
+//    mbarrier, waited on with a time limit. 99 KB of shared memory: two
 //    CTAs of 256 threads per SM.
 //  * Row p of the accumulator is tensor-memory lane p: warps w and w + 4
 //    read rows 32 (w % 4) .. + 31 (each half of the columns) with tcgen05.ld.
@@ -1267,10 +1269,10 @@ struct TCLay {
     static constexpr int kPart = 128 * 128 * 2;       // one bf16 operand: 128 rows x 128 tokens
     static constexpr int kA = 0;                      // w o U parts a1, a2
     static constexpr int kB = kA + kTCParts * kPart;  // B
-    static constexpr int kW = kB + kPart;
-    static constexpr int kW2 = kW + 128 * 4;
-    static constexpr int kDt = kW2 + 128 * 4;
-    static constexpr int kBytes = kDt + 128 * 4;
+    static constexpr int kW = kB + kPart;             // float[2][128]: per head of the tile (two at P = 64)
+    static constexpr int kW2 = kW + 2 * 128 * 4;
+    static constexpr int kDt = kW2 + 2 * 128 * 4;
+    static constexpr int kBytes = kDt + 2 * 128 * 4;
 };
 
 // K-major operand: row r (M or N index), token (K index) k.
@@ -1322,15 +1324,14 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
     unsigned char *sbytes = reinterpret_cast<unsigned char *>(ssm_smem);
     float *sw = sm<float>(TCLay::kW), *sw2 = sm<float>(TCLay::kW2), *sdt = sm<float>(TCLay::kDt);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // tile = 128 consecutive rows R = h P + p of the chunk's H P rows: one head, or two at P = 64 (same group)
     const long long t = blockIdx.x;
-    const int ptile = (int)(t % a.ptiles);
-    const long long vh = t / a.ptiles;
-    const int h = (int)(vh % a.H);
-    const long long v = vh / a.H;
-    const int gi = h / (a.H / a.G);
-    const int row0 = ptile * kTCRows;
+    const long long v = t / a.ptiles;
+    const int R0 = (int)(t % a.ptiles) * kTCRows;
+    const int h0 = R0 / a.P;
+    const int nh = a.P >= kTCRows ? 1 : 2;
+    const int gi = h0 / (a.H / a.G);
     constexpr int L = 128;
-    const float Ah = __ldg(a.A + h);
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(a.x);
     const __nv_bfloat16 *Bp = static_cast<const __nv_bfloat16 *>(a.B);
     const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
@@ -1341,14 +1342,16 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const long long bt = v * L + s0 + i;
-        xr[i] = __ldg(reinterpret_cast<const uint4 *>(x + (bt * a.H + h) * (long long)a.P + row0 + p0));
+        xr[i] = __ldg(reinterpret_cast<const uint4 *>(x + bt * a.H * (long long)a.P + R0 + p0));
         br[i] = __ldg(reinterpret_cast<const uint4 *>(Bp + (bt * a.G + gi) * 128LL + p0));
     }
-    // dt and the suffix products w_s = prod_{r > s} Abar_r (the product tree of ssm_chunk_state_kernel)
-    if (tid < L) {
-        const float d = ld1(dtp + (v * L + tid) * a.H + h);
+    // dt and the suffix products w_s = prod_{r > s} Abar_r (the product tree of ssm_chunk_state_kernel), per head
+    if (tid < nh * L) {
+        const int hh = h0 + (tid >> 7), s = tid & (L - 1);
+        const float Ah = __ldg(a.A + hh);
+        const float d = ld1(dtp + (v * L + s) * a.H + hh);
         sdt[tid] = d;
-        sw[tid] = tid + 1 < L ? ssm_decay(ld1(dtp + (v * L + tid + 1) * a.H + h), Ah) : 1.f;
+        sw[tid] = s + 1 < L ? ssm_decay(ld1(dtp + (v * L + s + 1) * a.H + hh), Ah) : 1.f;
     }
     if (tid == 0) {
         mbar_init(&bar, 1);
@@ -1371,18 +1374,19 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
     __syncthreads();
     float *cur = sw, *nxt = sw2;
     for (int d = 1; d < L; d <<= 1) {
-        if (tid < L) nxt[tid] = tid + d < L ? __fmul_rn(cur[tid], cur[tid + d]) : cur[tid];
+        if (tid < nh * L) nxt[tid] = (tid & (L - 1)) + d < L ? __fmul_rn(cur[tid], cur[tid + d]) : cur[tid];
         __syncthreads();
         float *tmp = cur;
         cur = nxt;
         nxt = tmp;
     }
-    // w o U in fp32, split into two bf16 parts, transposed into the A operands (row p0 + j)
+    // w o U in fp32, split into two bf16 parts, transposed into the A operands (row p0 + j, of head h0 + hf)
+    const int hf = nh == 1 ? 0 : p0 / a.P;
     float wsv[8], dsv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        wsv[i] = cur[s0 + i];
-        dsv[i] = sdt[s0 + i];
+        wsv[i] = cur[hf * L + s0 + i];
+        dsv[i] = sdt[hf * L + s0 + i];
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -1439,7 +1443,7 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
                 *reinterpret_cast<float4 *>(stage + r * kStagePitch + c0 + k) = make_float4(f[k], f[k + 1], f[k + 2], f[k + 3]);
         }
         __syncthreads();
-        float *out = a.ws + ((v * a.H + h) * (long long)a.P + row0) * 128;
+        float *out = a.ws + (v * a.H * (long long)a.P + R0) * 128;
 #pragma unroll 4
         for (int it = 0; it < 16; ++it) {
             const int idx = it * kTCThreads + tid, row = idx >> 5, c4 = (idx & 31) * 4;
@@ -2263,8 +2267,10 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     c1.dev_status = dev_status;
     const bool cs_ok = N <= 128 && P % kCSRows == 0 && aligned(x, 16) && aligned(B, 16) && (P * eb) % 16 == 0 &&
                        aligned(dt, eb);
-    // the tensor-memory form: bf16 inputs, N = 128, L = 128, 128-row tiles
-    const bool tc_ok = cs_ok && d->in_dtype == SSM_BF16 && N == 128 && L == 128 && P % kTCRows == 0;
+    // the tensor-memory form: bf16 inputs, N = 128, L = 128, tiles of 128 rows of one head, or of two heads of
+    // one group at P = 64
+    const bool tc_ok = cs_ok && d->in_dtype == SSM_BF16 && N == 128 && L == 128 &&
+                       (P % kTCRows == 0 || (P == 64 && (H / G) % 2 == 0));
     if (cs_ok) {
         CSArgs ca;
         ca.x = x;
@@ -2277,9 +2283,9 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         ca.P = (int)P;
         ca.G = (int)G;
         ca.L = L;
-        const int rows = tc_ok ? kTCRows : kCSRows;
-        ca.ptiles = (int)(P / rows);
-        const long long nt = (long long)dv.batch * H * (P / rows);
+        // tiles of a chunk: P / 64 per head, or H P / 128 over the chunk's rows on the tensor cores
+        ca.ptiles = tc_ok ? (int)(H * P / kTCRows) : (int)(P / kCSRows);
+        const long long nt = (long long)dv.batch * (tc_ok ? ca.ptiles : H * ca.ptiles);
         const cudaError_t e1 = tc_ok ? launch_chunk_state_tc(ca, nt, static_cast<cudaStream_t>(stream))
                                      : launch_chunk_state(d->in_dtype, (int)N, ca, nt, static_cast<cudaStream_t>(stream));
         if (e1 != cudaSuccess) {

@@ -305,3 +305,12 @@ def test_prefill_tensor_memory_64_row_tiles(cuda_device, P):
     128 (one and three tiles per head; the chunk states come from the mma.sync
     pass), bf16, N = 128, four 128-token chunks, against the oracle."""
     _prefill_case(cuda_device, 2, 4, P, 128, 2, 512, synth.BF16, seed=475 + P)
+
+
+@pytest.mark.parametrize("H,G", [(8, 1), (6, 2)])
+def test_prefill_tensor_memory_p64_head_pairs(cuda_device, H, G):
+    """P = 64: the tcgen05 chunk-state pass takes a 128-row tile over two heads
+    of one group (H / G even: w and dt differ per half, B is shared); with an
+    odd number of heads per group it keeps the mma.sync pass. Both against the
+    oracle."""
+    _prefill_case(cuda_device, 2, H, 64, 128, G, 384, synth.BF16, seed=480 + 7 * H + G)
