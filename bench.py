@@ -572,11 +572,19 @@ SM_COUNT, FP32_LANES, SM_MAX_GHZ = 148, 128, 2.032  # B300: the FP32 peak is der
 FP32_PEAK_TFLOPS = SM_COUNT * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
 
 
+# prompt shapes of the prefill bench: name -> (heads, headdim, dstate, ngroups)
+PREFILL_SHAPES = {
+    "llama3_8b": (32, 128, 128, 8),   # the distilled Llama-3-8B hybrid's Mamba layer
+    "mamba2_2p7b": (80, 64, 128, 1),  # a Mamba-2-2.7B layer
+}
+
+
 def run_prefill(args, rank, world, local_rank):
-    """Time ssm_prefill: one Llama-3-8B-shaped layer (H 32, P 128, N 128,
-    G 8), one 2048-token bf16 prompt per GPU, from a zeroed cache slot. The
-    algorithmic work is the recurrence over the prompt: 5 flops per state
-    element and token (u B, Abar h + u B, and y = C h)."""
+    """Time ssm_prefill: one layer of the chosen shape (default Llama-3-8B:
+    H 32, P 128, N 128, G 8; or Mamba-2-2.7B: H 80, P 64, N 128, G 1), one
+    2048-token bf16 prompt per GPU, from a zeroed cache slot. The algorithmic
+    work is the recurrence over the prompt: 5 flops per state element and
+    token (u B, Abar h + u B, and y = C h)."""
     import ssm_recurrence_verify_b300 as ssm
     from ssm_recurrence_verify_b300 import build as libbuild
     if not os.path.exists(libbuild.LIB):
@@ -584,7 +592,8 @@ def run_prefill(args, rank, world, local_rank):
     ssm.load_library()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = synth.custom_workload(1, 32, 128, 128, 8, 2048, synth.BF16, seed=500, accept="all")
+    H, P, N, G = PREFILL_SHAPES[args.prefill_shape]
+    wl = synth.custom_workload(1, H, P, N, G, 2048, synth.BF16, seed=500, accept="all")
     T = wl.ntok
     # inputs + y + state of one step; the workspace (shared) adds its own traffic
     step_bytes = T * (wl.nheads * wl.headdim * (2 + 4) + 2 * wl.ngroups * wl.dstate * 2 + wl.nheads * 2) \
@@ -644,7 +653,7 @@ def run_prefill(args, rank, world, local_rank):
         "metric": PREFILL_METRIC, "value": T * world / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": 3, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": "prefill_llama3_8b_layer_b1_t2048_h32_p128_n128_g8", "prompt_tokens": T,
+        "config": {"workload": f"prefill_{args.prefill_shape}_layer_b1_t{T}_h{H}_p{P}_n{N}_g{G}", "prompt_tokens": T,
                    "batch_per_gpu": 1, "in_dtype": "bf16", "workspace_bytes": nbytes,
                    "timing": f"{steps} launches captured in one CUDA graph",
                    "l2": f"{nsets} independent input sets rotated (each read again after > 2x the L2 of other traffic)"},
@@ -654,7 +663,8 @@ def run_prefill(args, rank, world, local_rank):
                      "algorithmic_flops_per_step": flops,
                      "hbm_gbs_on_io_bytes": io_bytes / (ms * 1e-3) / 1e9},
         "one_pass_ms": ms_one_pass,
-        "gpu_launches": steps, "clocks": sampler.summary(wall0, wall1),
+        # the chunked form is three kernels per prompt (chunk states, scan, outputs); the one pass is one
+        "gpu_launches": steps * (3 if nbytes > 0 else 1), "clocks": sampler.summary(wall0, wall1),
     }
 
 
@@ -767,6 +777,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill"], default="ssm",
                     help="ssm: the verify/commit step (default); accept_*: the acceptance step alone; "
                          "prefill: a 2048-token prompt through one layer")
+    ap.add_argument("--prefill-shape", choices=sorted(PREFILL_SHAPES), default="llama3_8b",
+                    help="layer shape of --path prefill")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

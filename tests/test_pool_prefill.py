@@ -184,6 +184,12 @@ def test_prefill_llama_layer_shape(cuda_device):
     _prefill_case(cuda_device, 1, 32, 128, 128, 8, 2048, synth.BF16, seed=461)
 
 
+def test_prefill_mamba2_layer_shape(cuda_device):
+    """A Mamba-2-2.7B-shaped layer (H 80, P 64, N 128, G 1), one 2048-token
+    prompt: the head-pair chunk-state tiles and the 64-row output tiles."""
+    _prefill_case(cuda_device, 1, 80, 64, 128, 1, 2048, synth.BF16, seed=464)
+
+
 def test_prefill_tensor_memory_chunk_states(cuda_device):
     """A shape whose chunk states take the tensor-memory (tcgen05) pass: bf16,
     N = 128, 128-token chunks, two 128-row tiles per head (P = 256)."""
