@@ -358,6 +358,27 @@ def test_layer_stack_validation(lib):
     assert lib.ssm_prefill_workspace_bytes(ctypes.byref(desc(nlayers=2, batch=1, ntok=2048))) == 0
 
 
+@no_gpu_only
+def test_prefill_chunk_rule_for_tensor_core_shapes(lib):
+    """bf16 prompts with N = 128, headdim a multiple of 64 and at least two
+    128-token chunks take 128-token chunks whatever the device: workspace =
+    batch * (T / 128) states + the chunks' slot map (16-byte rounded). Other
+    shapes chunk only to fill the device, which this host has none of (0)."""
+    def ws(**kw):
+        return lib.ssm_prefill_workspace_bytes(ctypes.byref(desc(**kw)))
+
+    def want(batch, T, H, P):
+        return batch * (T // 128) * H * P * 128 * 4 + (batch * (T // 128) * 4 + 15) // 16 * 16
+
+    for P in (64, 128, 192, 256):
+        assert ws(batch=1, nheads=80, headdim=P, ngroups=1, ntok=2048) == want(1, 2048, 80, P), P
+    assert ws(batch=3, nheads=4, headdim=64, ngroups=2, ntok=384) == want(3, 384, 4, 64)
+    for kw in (dict(headdim=96), dict(dstate=64), dict(in_dtype=sv.SSM_F32), dict(ntok=128), dict(ntok=2000)):
+        base = dict(batch=1, nheads=8, headdim=64, dstate=128, ngroups=1, ntok=2048)
+        base.update(kw)
+        assert ws(**base) == 0, kw
+
+
 def pool(states, slot=None, nslots=4, reserved=0):
     return sv.PoolDesc(states, slot, nslots, reserved)
 
