@@ -61,3 +61,32 @@ def test_slices_match_full_batch():
     for b, h in pairs:
         assert np.array_equal(sl[(b, h)]["y"], full["y"][b, :, h])
         assert np.array_equal(sl[(b, h)]["state"], full["state"][b, h])
+
+
+@pytest.mark.parametrize("L", [16, 12, 48])
+def test_chunked_regrouping_equals_recurrence(L):
+    """The regrouping the chunked prefill rests on, with the oracle alone:
+    every chunk's state from h = 0 (S_c), the chunk decays lambda_c (product
+    of the chunk's Abar = exp(dt A)), the carry H_c = lambda_c H_{c-1} + S_c
+    from the cached state, and each chunk's y from the state it starts from,
+    reproduce the token-by-token recurrence over the whole prompt."""
+    wl = synth.custom_workload(2, 3, 4, 8, 1, 48, synth.F32, seed=31)
+    d = synth.draw_layer_round(wl)
+    x, B, C, dt = (d[k].double().numpy() for k in ("x", "B", "C", "dt"))
+    A, D = d["A"].double().numpy(), d["D"].double().numpy()
+    h0 = d["state0"].double().numpy()
+    whole = oracle.verify_commit(h0, x, B, C, dt, A, D, None)
+    H = h0.copy()
+    ys = []
+    for c0 in range(0, 48, L):
+        sl = slice(c0, c0 + L)
+        S = oracle.verify_commit(np.zeros_like(h0), x[:, sl], B[:, sl], C[:, sl], dt[:, sl], A, D, None)["state"]
+        lam = np.prod(np.exp(dt[:, sl] * A[None, None, :]), axis=1)  # [batch][H]
+        ys.append(oracle.verify_commit(H, x[:, sl], B[:, sl], C[:, sl], dt[:, sl], A, D, None)["y"])
+        H = lam[:, :, None, None] * H + S
+    assert rel_err(np.concatenate(ys, axis=1), whole["y"]) < 1e-12
+    assert rel_err(H, whole["state"]) < 1e-12
+    # a dropped decay (lambda = 1) is caught
+    assert rel_err(sum(oracle.verify_commit(np.zeros_like(h0), x[:, c:c + L], B[:, c:c + L], C[:, c:c + L],
+                                            dt[:, c:c + L], A, D, None)["state"] for c in range(0, 48, L)) + h0,
+                   whole["state"]) > 1e-3
