@@ -1472,7 +1472,7 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
 //   Yc = M X      (M[t][s] = G[t][s] exp(A (cs_t - cs_s)) dt_s for s <= t,
 //                  else 0, split into two bf16 parts; x exact),
 // and y = w_t Yi + Yc + D x. One CTA of 256 threads per (chunk, head,
-// 128-row tile), two CTAs per SM: three 32 KB operand buffers are reused
+// row tile), two CTAs per SM: three 32 KB operand buffers are reused
 // phase by phase (C and B, then the low part of H0 over B, then M over H0
 // and C with x over B), and Yc accumulates in G's tensor-memory columns once
 // G has been read, so a CTA needs 97 KB of shared memory and 256 columns.
