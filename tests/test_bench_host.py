@@ -1,0 +1,92 @@
+"""Host-side pieces of the benchmark on CPU: the algorithmic byte count of
+one layer-call, the clock summary's window and reason decoding, the tile
+kernel's source hash (which decides whether a recorded traffic capture still
+applies) and the measured-peak lookup."""
+import json
+import os
+
+import bench
+from ssm_recurrence_verify_b300 import synth
+
+
+def test_algorithmic_bytes_by_hand():
+    """batch 2, H 3, P 4, N 8, G 1, K 5, bf16: the state read for both
+    sequences, written for the one with j > 0; x, B, C, dt read once (B and C
+    once per group); y written in fp32; accept_len read."""
+    wl = synth.custom_workload(2, 3, 4, 8, 1, 5, synth.BF16, seed=1)
+    state = 3 * 4 * 8 * 4                        # one sequence's fp32 state: 384 B
+    per_token = 3 * 4 * 2 + 2 * 1 * 8 * 2 + 3 * 2  # x, B and C, dt in bf16: 62 B
+    y = 3 * 4 * 4                                # fp32 y per token: 48 B
+    want = 2 * state + 1 * state + 2 * 5 * (per_token + y) + 2 * 4
+    assert bench.algorithmic_bytes(wl, 2, 1) == want == 2260
+
+
+def test_algorithmic_bytes_accept_all_reads_no_accept_len():
+    wl = synth.custom_workload(1, 1, 8, 16, 1, 4, synth.F32, seed=1, accept="all")
+    state = 8 * 16 * 4
+    assert bench.algorithmic_bytes(wl, 1, 1) == 2 * state + 4 * (8 * 4 + 2 * 16 * 4 + 4 + 8 * 4)
+
+
+def _sampler(samples, max_mhz=2032.0, mode="nvml"):
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples, s.max_mhz, s.mode, s.err = samples, max_mhz, mode, ""
+    return s
+
+
+def test_clock_summary_window_and_reasons():
+    # (time, SM MHz, reason bits): only the samples inside [1, 2] count
+    s = _sampler([(0.5, 900.0, 0x8), (1.0, 2032.0, 0x0), (1.5, 2000.0, 0x4), (2.0, 1990.0, 0x0),
+                  (2.5, 800.0, 0x80)])
+    out = s.summary(1.0, 2.0)
+    assert out["sm_mhz"] == 2000.0 and out["samples"] == 3 and out["sm_max_mhz"] == 2032.0
+    assert out["reasons"] == ["sw_power_cap"]  # the hw_slowdown and thermal bits fall outside the window
+    assert "timed region" in out["note"]
+
+
+def test_clock_summary_decodes_every_reason_bit():
+    s = _sampler([(1.0, 1500.0, 0x4 | 0x8 | 0x40 | 0x80)])
+    assert s.summary(0.0, 2.0)["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap",
+                                              "sw_thermal_slowdown"]
+
+
+def test_clock_summary_short_window_and_no_source():
+    s = _sampler([(0.1, 2032.0, 0), (0.3, 2032.0, 0)], mode="nvidia-smi")
+    out = s.summary(0.15, 0.2)  # shorter than the sampling period: every sample is used, and says so
+    assert out["samples"] == 2 and "shorter than the sampling period" in out["note"]
+    none = _sampler([], mode=None)
+    none.err = "nvml: missing"
+    assert none.summary(0.0, 1.0)["sm_mhz"] is None
+
+
+def test_kernel_source_hash_covers_the_tile_kernel_only(tmp_path):
+    """Edits after the prefill marker, and #include lines, leave the hash
+    unchanged; an edit of the tile kernel's code changes it."""
+    src = ("#include <a.h>\n__global__ void tile() { int a = 1; }\n" + bench.PREFILL_MARKER +
+           "\n__global__ void prefill() {}\n")
+    p = tmp_path / "k.cu"
+    p.write_text(src)
+    h0 = bench.kernel_source_hash(str(p))
+    p.write_text(src.replace("#include <a.h>", "#include <b.h>").replace("prefill() {}", "prefill() { x(); }"))
+    assert bench.kernel_source_hash(str(p)) == h0
+    p.write_text(src.replace("int a = 1", "int a = 2"))
+    assert bench.kernel_source_hash(str(p)) != h0
+
+
+def test_recorded_traffic_matches_the_current_tile_kernel():
+    """The committed capture of the headline workload was taken on the tile
+    kernel as it stands (otherwise the bench reports traffic as null)."""
+    name = "batched_spec_serving_b64_h32_p128_n128_g8_k8"
+    with open(os.path.join(bench.PROFILES, f"ssm_tile_kernel_{name}.traffic.json")) as f:
+        rec = json.load(f)
+    assert rec["kernel_source_sha256"] == bench.kernel_source_hash()
+    assert bench.recorded_traffic(name) == rec["dram_bytes_per_launch"] > 0
+
+
+def test_hbm_peak_reads_the_measured_file():
+    value, source = bench.hbm_peak()
+    path = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            assert (value, source) == (float(json.load(f)["hbm_gbs"]), "measured")
+    else:
+        assert (value, source) == (bench.FALLBACK_HBM_GBS, "fallback")
