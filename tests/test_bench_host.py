@@ -1,9 +1,11 @@
 """Host-side pieces of the benchmark on CPU: the algorithmic byte count of
 one layer-call, the clock summary's window and reason decoding, the tile
 kernel's source hash (which decides whether a recorded traffic capture still
-applies) and the measured-peak lookup."""
+applies), the measured-peak lookup and the layer-stack input sets."""
 import json
 import os
+
+import torch
 
 import bench
 from ssm_recurrence_verify_b300 import synth
@@ -90,3 +92,29 @@ def test_hbm_peak_reads_the_measured_file():
             assert (value, source) == (float(json.load(f)["hbm_gbs"]), "measured")
     else:
         assert (value, source) == (bench.FALLBACK_HBM_GBS, "fallback")
+
+
+def test_layer_set_shards_views_and_shared_accept_len():
+    """The bench's layer-stack input set on CPU: a rank's shard equals its
+    slice of the single-process stack, every layer's draw has the same
+    accept_len (the stack shares one per sequence), and the per-layer views
+    alias the stacked slabs, so per-layer and stacked launches read the same
+    memory."""
+    wl = synth.custom_workload(4, 2, 8, 16, 1, 3, synth.BF16, seed=9)
+    full = bench.LayerSet(wl, 4, 0, 0, "cpu", 3)
+    for rank in (0, 1):
+        batch, offset = bench.shard(2, rank)
+        part = bench.LayerSet(wl, batch, offset, 0, "cpu", 3)
+        for k in ("state0", "x", "B", "C", "dt"):
+            assert torch.equal(part.stack[k], full.stack[k][:, offset:offset + batch]), (rank, k)
+        for k in ("A", "D"):
+            assert torch.equal(part.stack[k], full.stack[k]), (rank, k)
+        assert torch.equal(part.stack["accept_len"], full.stack["accept_len"][offset:offset + batch])
+    for layer, e in enumerate(full.layers):
+        assert torch.equal(e["host"]["accept_len"], full.stack["accept_len"])
+        for k in ("state0", "x", "y"):
+            assert e[k].data_ptr() == full.stack[k][layer].data_ptr(), (layer, k)
+        assert e["accepted_nonzero"] == int((full.stack["accept_len"] > 0).sum())
+    # the layers differ in their parameters and inputs
+    assert not torch.equal(full.stack["A"][0], full.stack["A"][1])
+    assert not torch.equal(full.stack["x"][0], full.stack["x"][1])
