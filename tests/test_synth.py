@@ -44,3 +44,28 @@ def test_accept_recipe_structure():
     assert float(u.min()) >= 0.0 and float(u.max()) < 1.0
     bf = synth.draw_accept_inputs(synth.custom_accept_workload(2, 4, 500, synth.BF16))
     assert bf["target_logits"].dtype == torch.bfloat16
+
+
+def test_draw_recipe_distributions():
+    """The stated input recipe: state0 ~ N(0, 0.1) (std 0.1), x, B, C ~ N(0, 1/N),
+    dt = softplus(N(-2, 1)) > 0, A = -exp(U(0, ln 16)) in [-16, -1], and
+    accept_len = tokens accepted before the first rejection with rejection
+    probability 0.3, capped at K (P(0) = 0.3, E = sum_{k=1..K} 0.7^k)."""
+    wl = synth.custom_workload(4000, 8, 4, 64, 1, 16, synth.F32, seed=77, accept="geometric")
+    acc = synth.draw_accept_len(wl).double()
+    assert abs(float((acc == 0).double().mean()) - 0.3) < 0.025
+    want_mean = sum(0.7 ** k for k in range(1, 17))
+    assert abs(float(acc.mean()) - want_mean) < 0.15  # about 3.4 standard errors at 4000 draws
+    assert int(acc.max()) == 16 and int(acc.min()) == 0
+    small = synth.custom_workload(64, 8, 4, 64, 1, 16, synth.F32, seed=77)
+    p = synth.draw_params(small)
+    assert abs(float(p["state0"].std()) - 0.1) < 0.005
+    assert float(p["A"].max()) <= -1.0 and float(p["A"].min()) >= -16.0
+    t = synth.draw_tokens(small)
+    for k in ("x", "B", "C"):
+        assert abs(float(t[k].std()) - 1 / 8) < 0.01, k  # 1 / sqrt(N), N = 64
+    assert float(t["dt"].min()) > 0.0
+    raw = torch.log(torch.expm1(t["dt"].double()))  # the pre-softplus normal
+    assert abs(float(raw.mean()) + 2.0) < 0.1 and abs(float(raw.std()) - 1.0) < 0.1
+    u = synth.draw_accept_len(synth.custom_workload(4000, 1, 1, 1, 1, 8, seed=3))
+    assert int(u.min()) == 0 and int(u.max()) == 8 and abs(float(u.double().mean()) - 4.0) < 0.2
