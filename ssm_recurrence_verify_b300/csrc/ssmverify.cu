@@ -2269,7 +2269,7 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
                        aligned(dt, eb);
     // the tensor-memory form: bf16 inputs, N = 128, L = 128, tiles of 128 rows of one head, or of two heads of
     // one group at P = 64
-    const bool tc_ok = cs_ok && d->in_dtype == SSM_BF16 && N == 128 && L == 128 &&
+    const bool tc_states = cs_ok && d->in_dtype == SSM_BF16 && N == 128 && L == 128 &&
                        (P % kTCRows == 0 || (P == 64 && (H / G) % 2 == 0));
     if (cs_ok) {
         CSArgs ca;
@@ -2284,9 +2284,9 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         ca.G = (int)G;
         ca.L = L;
         // tiles of a chunk: P / 64 per head, or H P / 128 over the chunk's rows on the tensor cores
-        ca.ptiles = tc_ok ? (int)(H * P / kTCRows) : (int)(P / kCSRows);
-        const long long nt = (long long)dv.batch * (tc_ok ? ca.ptiles : H * ca.ptiles);
-        const cudaError_t e1 = tc_ok ? launch_chunk_state_tc(ca, nt, static_cast<cudaStream_t>(stream))
+        ca.ptiles = tc_states ? (int)(H * P / kTCRows) : (int)(P / kCSRows);
+        const long long nt = (long long)dv.batch * (tc_states ? ca.ptiles : H * ca.ptiles);
+        const cudaError_t e1 = tc_states ? launch_chunk_state_tc(ca, nt, static_cast<cudaStream_t>(stream))
                                      : launch_chunk_state(d->in_dtype, (int)N, ca, nt, static_cast<cudaStream_t>(stream));
         if (e1 != cudaSuccess) {
             g_last_cuda_error = (int)e1;
