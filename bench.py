@@ -692,6 +692,63 @@ def oracle_throughput(wl, seconds: float, max_seqs: int = None):
                        f"({wl.nheads} heads, P {wl.headdim}, N {wl.dstate}), fp64, {el:.1f} s")
 
 
+def oracle_throughput_threads(wl, seconds: float, threads: int):
+    """The same fp64 oracle, as it stands, on `threads` host threads at once:
+    thread i runs full passes over sequence i (mod the batch) of the
+    workload's first layer until `seconds` have elapsed. The C recurrence runs
+    outside the GIL (ctypes releases it for the call), so the threads occupy
+    that many cores. Returns (tokens per second, description)."""
+    import concurrent.futures
+    import oracle
+    args = []
+    for i in range(threads):
+        d = synth.draw_layer_round(wl, batch=1, batch_offset=i % wl.batch)
+        args.append((d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"],
+                     None if wl.accept == "all" else d["accept_len"]))
+    start = threading.Barrier(threads + 1)
+
+    def work(a):
+        start.wait(timeout=120)
+        t0, reps = time.perf_counter(), 0
+        while True:
+            oracle.verify_commit(*a)
+            reps += 1
+            if time.perf_counter() - t0 >= seconds:
+                return reps
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = [ex.submit(work, a) for a in args]
+        start.wait(timeout=120)
+        t0 = time.perf_counter()
+        reps = [f.result() for f in futs]
+        el = time.perf_counter() - t0
+    toks = sum(reps) * wl.ntok
+    return toks / el, (f"{threads} threads at once, thread i over sequence i mod {wl.batch}: {sum(reps)} full oracle "
+                       f"passes of one sequence x {wl.ntok} draft tokens of one layer ({wl.nheads} heads, "
+                       f"P {wl.headdim}, N {wl.dstate}), fp64, {el:.1f} s")
+
+
+def host_cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def host_threads(cap: int = 64) -> int:
+    """Cores this process may run on (its affinity set), at most `cap`."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(cap, n))
+
+
 def reference_sample(wl, per_unit_s: float, steps: int):
     """Pick (sequences, heads) per oracle step so that `steps` steps take
     about two minutes. The smallest unit is one sequence and one B/C group's
@@ -768,6 +825,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads for the second, multi-threaded oracle timing (0: the cores this process "
+                         "may use, at most 64; 1: skip it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--layers", type=int, default=None,
@@ -808,10 +868,16 @@ def main(argv=None):
         return 0
     r = run_ours(args, wl, rank, world, local_rank)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample = oracle_throughput(wl, args.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "cpu_model": host_cpu_model()}
+        nt = host_threads() if args.cpu_threads == 0 else args.cpu_threads
+        if nt > 1:
+            v, sample = oracle_throughput_threads(wl, args.cpu_seconds, nt)
+            cpu_all = {"value": v, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": sample,
+                       "cpu_model": cpu["cpu_model"]}
 
     if rank == 0:
         traffic = recorded_traffic(wl.name)
@@ -827,6 +893,7 @@ def main(argv=None):
                          "launch_us_mean": r["launch_ms_mean"] * 1e3,
                          "frac_of_8tbs_spec": r["achieved_gbs"] / HBM_SPEC_GBS},
             "cpu_baseline": cpu,
+            "cpu_baseline_threads": cpu_all,
             "e2e": r["e2e"],
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],

@@ -1,7 +1,8 @@
 """Host-side pieces of the benchmark on CPU: the algorithmic byte count of
 one layer-call, the clock summary's window and reason decoding, the tile
 kernel's source hash (which decides whether a recorded traffic capture still
-applies), the measured-peak lookup and the layer-stack input sets."""
+applies), the measured-peak lookup, the layer-stack input sets and the
+multi-threaded oracle timing."""
 import json
 import os
 
@@ -118,3 +119,13 @@ def test_layer_set_shards_views_and_shared_accept_len():
     # the layers differ in their parameters and inputs
     assert not torch.equal(full.stack["A"][0], full.stack["A"][1])
     assert not torch.equal(full.stack["x"][0], full.stack["x"][1])
+
+
+def test_oracle_timing_on_several_threads():
+    """The multi-threaded oracle baseline runs every thread's passes and
+    credits their tokens; the host's thread count is its affinity set, capped."""
+    wl = synth.WORKLOADS[0]
+    v, sample = bench.oracle_throughput_threads(wl, 0.2, 3)
+    assert v > 0 and sample.startswith("3 threads at once")
+    assert 1 <= bench.host_threads() <= 64 and bench.host_threads(cap=1) == 1
+    assert isinstance(bench.host_cpu_model(), str)
