@@ -874,8 +874,8 @@ def main(argv=None):
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
                "cpu_model": host_cpu_model()}
         nt = host_threads() if args.cpu_threads == 0 else args.cpu_threads
-        if nt > 1:
-            v, sample = oracle_throughput_threads(wl, args.cpu_seconds, nt)
+        if nt > 1:  # a window that keeps the CPU work near 2 x cpu_seconds however many threads run
+            v, sample = oracle_throughput_threads(wl, max(0.5, 2.0 * args.cpu_seconds / nt), nt)
             cpu_all = {"value": v, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": sample,
                        "cpu_model": cpu["cpu_model"]}
 
