@@ -129,3 +129,23 @@ def test_oracle_timing_on_several_threads():
     assert v > 0 and sample.startswith("3 threads at once")
     assert 1 <= bench.host_threads() <= 64 and bench.host_threads(cap=1) == 1
     assert isinstance(bench.host_cpu_model(), str)
+
+
+def test_json_line_assembly_with_the_device_leg_stubbed(monkeypatch, capsys):
+    """main() on a host without a GPU, its device leg replaced by fixed
+    numbers: one JSON line with the contract's keys, both oracle baselines
+    (one thread, then several) and the roofline fraction computed from them."""
+    fake = {"value": 1.0e6, "ms_per_step": 0.5, "nsets": 3, "layers_per_launch": 1, "achieved_gbs": 4000.0,
+            "peak": 6400.0, "peak_kind": "measured", "bytes_per_launch": 2.0e6, "launch_ms_mean": 0.5,
+            "e2e": None, "launches": 7, "clocks": {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}}
+    monkeypatch.setattr(bench, "run_ours", lambda *a: fake)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    assert bench.main(["--workload", "0", "--cpu-seconds", "0.2", "--cpu-threads", "2"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert k in line, k
+    assert line["roofline"]["frac"] == 4000.0 / 6400.0 and line["roofline"]["bound"] == "hbm"
+    assert line["cpu_baseline"]["cores"] == 1 and line["cpu_baseline"]["value"] > 0
+    assert line["cpu_baseline_threads"]["cores"] == 2 and line["cpu_baseline_threads"]["value"] > 0
+    assert line["config"]["workload"] == synth.WORKLOADS[0].name and line["gpu_launches"] == 7
