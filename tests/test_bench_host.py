@@ -149,3 +149,26 @@ def test_json_line_assembly_with_the_device_leg_stubbed(monkeypatch, capsys):
     assert line["cpu_baseline"]["cores"] == 1 and line["cpu_baseline"]["value"] > 0
     assert line["cpu_baseline_threads"]["cores"] == 2 and line["cpu_baseline_threads"]["value"] > 0
     assert line["config"]["workload"] == synth.WORKLOADS[0].name and line["gpu_launches"] == 7
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """`bench.py --impl reference` (the fp64 oracle on the host cores, no GPU):
+    one JSON line on the same metric and config as the device arm, with its
+    own cpu_baseline and an e2e that copies nothing."""
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    assert bench.main(["--impl", "reference", "--workload", "0", "--steps", "3", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "tokens/s"
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["value"] > 0 and line["higher_is_better"]
+    assert line["config"]["workload"] == synth.WORKLOADS[0].name
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--workload", "0", "--steps", "3", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out.strip() == ""
