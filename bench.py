@@ -705,6 +705,7 @@ def oracle_throughput_threads(wl, seconds: float, threads: int):
         d = synth.draw_layer_round(wl, batch=1, batch_offset=i % wl.batch)
         args.append((d["state0"], d["x"], d["B"], d["C"], d["dt"], d["A"], d["D"],
                      None if wl.accept == "all" else d["accept_len"]))
+    oracle.verify_commit(*args[0])  # the library loaded (or built) once, before the threads start
     start = threading.Barrier(threads + 1)
 
     def work(a):
