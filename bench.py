@@ -741,12 +741,34 @@ def host_cpu_model() -> str:
     return platform.processor() or "unknown"
 
 
+def cgroup_cpu_limit(path: str = "/sys/fs/cgroup/cpu.max"):
+    """Whole cores a cgroup-v2 CPU quota allows ("quota period"), or None when unlimited or absent."""
+    try:
+        with open(path) as f:
+            quota, period = f.read().split()[:2]
+        if quota == "max":
+            return None
+        return max(1, int(int(quota) // int(period)))
+    except (OSError, ValueError):
+        return None
+
+
 def host_threads(cap: int = 64) -> int:
-    """Cores this process may run on (its affinity set), at most `cap`."""
+    """Cores this process may run on: its affinity set, within the cgroup's CPU quota, at most `cap`."""
     try:
         n = len(os.sched_getaffinity(0))
     except AttributeError:
         n = os.cpu_count() or 1
+    q = cgroup_cpu_limit()
+    if q is None:  # cgroup v1: quota and period in two files, -1 = unlimited
+        try:
+            with open("/sys/fs/cgroup/cpu/cpu.cfs_quota_us") as fq, open("/sys/fs/cgroup/cpu/cpu.cfs_period_us") as fp:
+                quota, period = int(fq.read()), int(fp.read())
+            q = max(1, quota // period) if quota > 0 and period > 0 else None
+        except (OSError, ValueError):
+            q = None
+    if q is not None:
+        n = min(n, q)
     return max(1, min(cap, n))
 
 

@@ -172,3 +172,14 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--workload", "0", "--steps", "3", "--warmup", "3"]) == 0
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_cgroup_cpu_limit(tmp_path):
+    f = tmp_path / "cpu.max"
+    f.write_text("800000 100000\n")
+    assert bench.cgroup_cpu_limit(str(f)) == 8
+    f.write_text("150000 100000\n")
+    assert bench.cgroup_cpu_limit(str(f)) == 1
+    f.write_text("max 100000\n")
+    assert bench.cgroup_cpu_limit(str(f)) is None
+    assert bench.cgroup_cpu_limit(str(tmp_path / "absent")) is None
