@@ -373,6 +373,10 @@ def test_prefill_chunk_rule_for_tensor_core_shapes(lib):
     for P in (64, 128, 192, 256):
         assert ws(batch=1, nheads=80, headdim=P, ngroups=1, ntok=2048) == want(1, 2048, 80, P), P
     assert ws(batch=3, nheads=4, headdim=64, ngroups=2, ntok=384) == want(3, 384, 4, 64)
+    # one 2048-token prompt of a Llama-3-8B or a Mamba-2-2.7B layer fits the library's fixed scratch, so
+    # ssm_prefill_scratch takes the same 128-token chunks as a caller workspace would
+    for H, P, G in ((32, 128, 8), (80, 64, 1)):
+        assert 0 < ws(batch=1, nheads=H, headdim=P, ngroups=G, ntok=2048) <= sv.SSM_PREFILL_SCRATCH_BYTES
     for kw in (dict(headdim=96), dict(dstate=64), dict(in_dtype=sv.SSM_F32), dict(ntok=128), dict(ntok=2000)):
         base = dict(batch=1, nheads=8, headdim=64, dstate=128, ngroups=1, ntok=2048)
         base.update(kw)
