@@ -263,15 +263,22 @@ int ssm_prefill(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, c
 /*
  * ssm_prefill_scratch -- ssm_prefill without a caller workspace: the chunked
  * form runs in a fixed device array of SSM_PREFILL_SCRATCH_BYTES inside the
- * library (allocated with the library's device code, once per device). The
+ * library (part of the library's device code: each CUDA context that loads
+ * the library holds one copy until it is destroyed). The
  * chunk length is chosen among those whose workspace fits in the array;
  * where none fits the one-pass form runs (it needs no workspace, but takes
  * the prompt token after token), so results equal ssm_prefill's with a
  * workspace of SSM_PREFILL_SCRATCH_BYTES. Nothing in the array needs to start
- * at zero. Calls that may overlap in time (other
- * streams, other host threads, other processes sharing the context) race on
- * the array: issue them one after another. The pages have no counterpart;
- * this exists for callers that cannot allocate device memory.
+ * at zero. Calls in the same CUDA context that may overlap on the device
+ * (issued on other streams, from other host threads, or while an earlier
+ * call still runs on another stream) race on the array: order them on one
+ * stream. (Each context has its own copy of the array.) The array's device
+ * address is looked up on every call, so the call stays correct after
+ * cudaDeviceReset. The pages have no counterpart; this exists for callers
+ * that cannot allocate device memory: a host runtime that owns every device
+ * allocation itself and hands this library only its tensors' pointers, or a
+ * latency-critical serving loop that must not enter cudaMalloc (which can
+ * synchronise the device) between steps.
  */
 #define SSM_PREFILL_SCRATCH_BYTES (64ll << 20)
 int ssm_prefill_scratch(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x, const void *B, const void *C,

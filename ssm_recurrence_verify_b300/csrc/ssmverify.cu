@@ -1835,8 +1835,9 @@ __global__ void __launch_bounds__(kScanThreads, 4) ssm_chunk_scan_kernel(const S
 }
 
 // Fixed device scratch of ssm_prefill_scratch: the chunked prefill's
-// workspace for callers that do not allocate one. Calls using it must not
-// overlap in time: they would share it.
+// workspace for callers that do not allocate one. Every call in one CUDA
+// context shares it, so calls that may overlap on the device (other streams,
+// other host threads, a call still running) race on it.
 static __device__ __align__(256) unsigned char g_prefill_scratch[SSM_PREFILL_SCRATCH_BYTES];
 
 // ----------------------------------------------------------------------------- host side
@@ -2360,19 +2361,15 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
     return run(&dv, c3, stream);
 }
 
-// Device address of the prefill scratch on the current device (cached per device).
+// Device address of the prefill scratch in the current context. It is looked
+// up on every call, not cached: after cudaDeviceReset, or in another context
+// on the same device, the library's device code is loaded again and the array
+// may sit elsewhere, so a remembered address could point at unmapped or
+// foreign memory. The lookup is cheap next to the kernels it feeds.
 void *prefill_scratch(cudaError_t &err) {
-    static std::atomic<void *> cache[kMaxDevices];
-    int dev = 0;
-    err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return nullptr;
-    void *p = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : nullptr;
-    if (p == nullptr) {
-        err = cudaGetSymbolAddress(&p, g_prefill_scratch);
-        if (err != cudaSuccess) return nullptr;
-        if (dev >= 0 && dev < kMaxDevices) cache[dev].store(p, std::memory_order_relaxed);
-    }
-    return p;
+    void *p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_prefill_scratch);
+    return err == cudaSuccess ? p : nullptr;
 }
 
 Call pool_call(int flavour, const ssm_pool_t *pool) {

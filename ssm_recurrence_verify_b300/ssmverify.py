@@ -454,9 +454,12 @@ def prefill(states, slot, x, B, C, dt, A, D, y=None, workspace=None, dev_status=
 
 def prefill_scratch(states, slot, x, B, C, dt, A, D, y=None, dev_status=None, stream=None) -> torch.Tensor:
     """prefill with the library's fixed device scratch as the workspace
-    (nothing is allocated for it). Calls must not overlap in time; the
-    chunk length is limited to those whose workspace fits in
-    SSM_PREFILL_SCRATCH_BYTES, else the one-pass form runs."""
+    (the library allocates nothing for it; y is allocated here only when the
+    caller passes none). For callers that cannot allocate device memory.
+    Calls in one CUDA context that may overlap on the device share the
+    scratch and race: order them on one stream. The chunk length is limited
+    to those whose workspace fits in SSM_PREFILL_SCRATCH_BYTES, else the
+    one-pass form runs."""
     y = _new_y(states, x) if y is None else y
     desc, _ = _validate(states, x, B, C, dt, A, D, None, y, pooled=True)
     pool = _pool(states, slot, desc.batch)

@@ -1,8 +1,12 @@
 """ssm_prefill_scratch (the prefill that runs its chunked form in the
 library's fixed device scratch) against ssm_prefill with a caller workspace,
 on two consecutive calls: the same chunk length is chosen, so the results
-agree bit for bit. Collected last on purpose: it must also pass after every
-other test has run in the same process."""
+agree bit for bit. The entry point serves callers that cannot allocate
+device memory: a host runtime that owns every device allocation and passes
+the library only tensor pointers, or a serving loop that must not call
+cudaMalloc (it can synchronise the device) between steps. Collected last on
+purpose: it must also pass after every other test has run in the same
+process."""
 import pytest
 import torch
 
