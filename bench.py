@@ -18,8 +18,13 @@ and replayed back to back, as a serving loop runs its layers; CUDA events on
 the launching stream time the whole region, and the average launch duration
 is that time over the launches.
 
-Under torchrun every rank runs its own sequences (weak scaling, no collective
-in the data path); the elapsed time is the maximum over ranks.
+With --gpus N, N ranks run, one per GPU: started by an outside launcher
+(torchrun sets RANK / WORLD_SIZE / LOCAL_RANK / MASTER_*), or else spawned by
+this script itself. Rank r owns sequences [r B, (r + 1) B) of a global batch
+of N B (weak scaling: B sequences per GPU, drawn from the same seeded streams
+as a single-process run of N B sequences); the data path has no collective.
+The elapsed time is the maximum over ranks, and the value counts every
+rank's sequences.
 
 --impl reference times the fp64 CPU oracle (the only reference there is) on
 bounded samples of the same workload, on rank 0 only.
@@ -84,6 +89,43 @@ def barrier(world: int):
         dist.barrier()
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_entry(rank: int, world: int, port: int, argv, entry):
+    """One spawned rank: the environment torchrun would set, then the bench."""
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world), LOCAL_WORLD_SIZE=str(world),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    rc = (main if entry is None else entry)(list(argv))
+    if rc:
+        raise SystemExit(rc)
+
+
+def launch_ranks(argv, world: int, entry=None) -> int:
+    """`--gpus N` without an outside launcher: start N ranks on this node, one
+    process per GPU (rank r on GPU r), by spawn (a fresh interpreter each, so
+    no CUDA state is forked), with the rendezvous on 127.0.0.1. Rank 0 prints
+    the JSON line. `entry` replaces main in the ranks (tests)."""
+    import torch.multiprocessing as mp
+    mp.spawn(_rank_entry, args=(world, free_port(), list(argv), entry), nprocs=world, join=True)
+    return 0
+
+
+def init_ranks(world: int, local_rank: int):
+    """The process group of a multi-rank run: NCCL on GPUs; gloo where no GPU
+    is visible (host-side runs of the timing logic). Only the max-over-ranks
+    reduction and the barriers use it: the data path has no collective."""
+    import torch.distributed as dist
+    if torch.cuda.is_available():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    else:
+        dist.init_process_group("gloo")
+
+
 # ----------------------------------------------------------------------------- bytes per launch
 
 def algorithmic_bytes(wl: synth.Workload, batch: int, accepted_nonzero: int) -> int:
@@ -109,10 +151,59 @@ def physical_gpu(local_rank: int) -> str:
     return str(local_rank)
 
 
+class NvmlCtypes:
+    """The few NVML calls the clock sampler makes, straight from the
+    driver's libnvidia-ml through ctypes (for hosts without the pynvml
+    package). Same names and return values as pynvml; raises on an error."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._call("nvmlInit_v2")
+
+    def _call(self, name, *args):
+        rc = getattr(self.lib, name)(*args)
+        if rc != 0:
+            raise RuntimeError(f"{name} returned NVML error {rc}")
+
+    def nvmlDeviceGetHandleByIndex(self, index):
+        h = self.ct.c_void_p()
+        self._call("nvmlDeviceGetHandleByIndex_v2", self.ct.c_uint(index), self.ct.byref(h))
+        return h
+
+    def nvmlDeviceGetHandleByUUID(self, uuid):
+        h = self.ct.c_void_p()
+        self._call("nvmlDeviceGetHandleByUUID", self.ct.c_char_p(uuid.encode()), self.ct.byref(h))
+        return h
+
+    def _clock(self, name, h, kind):
+        v = self.ct.c_uint()
+        self._call(name, h, self.ct.c_int(kind), self.ct.byref(v))
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._clock("nvmlDeviceGetClockInfo", h, kind)
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._clock("nvmlDeviceGetMaxClockInfo", h, kind)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.ct.c_ulonglong()
+        name = ("nvmlDeviceGetCurrentClocksEventReasons" if hasattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons")
+                else "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._call(name, h, self.ct.byref(v))
+        return v.value
+
+
 class ClockSampler:
     """Samples the SM clock and clock-event reasons during a window, through
-    NVML in a thread, or through a `nvidia-smi -lms` subprocess where the
-    NVML binding is not installed."""
+    NVML in a thread (the pynvml package, else the driver's libnvidia-ml via
+    ctypes), or through a `nvidia-smi -lms` subprocess where neither loads.
+    A polling nvidia-smi subprocess measurably slowed the timed kernels
+    (about 2 % at a 20 ms period); the in-process NVML thread is preferred."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x40: "sw_thermal_slowdown",
                0x80: "hw_thermal_slowdown", 0x100: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
@@ -125,19 +216,29 @@ class ClockSampler:
         self.err = ""
         self.mode = None
         self._stop = threading.Event()
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = (pynvml.nvmlDeviceGetHandleByUUID(self.gpu) if self.gpu.startswith(("GPU-", "MIG-"))
-                      else pynvml.nvmlDeviceGetHandleByIndex(int(self.gpu)))
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.mode = "nvml"
-        except Exception as e:
-            self.err = f"nvml: {e}"
+        errs = []
+        for opener in (self._pynvml, NvmlCtypes):
+            try:
+                nv = opener()
+                self.h = (nv.nvmlDeviceGetHandleByUUID(self.gpu) if self.gpu.startswith(("GPU-", "MIG-"))
+                          else nv.nvmlDeviceGetHandleByIndex(int(self.gpu)))
+                self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+                self.nv = nv
+                self.mode = "nvml" if opener is not NvmlCtypes else "nvml-ctypes"
+                break
+            except Exception as e:
+                errs.append(f"{getattr(opener, '__name__', 'nvml')}: {e}")
+        if self.mode is None:
+            self.err = "; ".join(errs)
             import shutil
             if shutil.which("nvidia-smi"):
                 self.mode = "nvidia-smi"
+
+    @staticmethod
+    def _pynvml():
+        import pynvml
+        pynvml.nvmlInit()
+        return pynvml
 
     def _nvml_loop(self):
         f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
@@ -162,7 +263,7 @@ class ClockSampler:
                 continue
 
     def start(self):
-        if self.mode == "nvml":
+        if self.mode in ("nvml", "nvml-ctypes"):
             self.t = threading.Thread(target=self._nvml_loop, daemon=True)
             self.t.start()
         elif self.mode == "nvidia-smi":
@@ -176,7 +277,7 @@ class ClockSampler:
             time.sleep(0.3)  # let the first samples arrive
 
     def stop(self):
-        if self.mode == "nvml":
+        if self.mode in ("nvml", "nvml-ctypes"):
             self._stop.set()
             self.t.join()
         elif self.mode == "nvidia-smi":
@@ -245,6 +346,20 @@ def recorded_traffic(workload_name: str):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def upload_graphs(graphs, stream):
+    """Upload each instantiated graph to the device (cudaGraphUpload) without
+    running it, so that the first replay inside a timed region does not also
+    pay the graph's upload: with a 20-step region that one-time cost moved the
+    mean step time by about 2 %."""
+    from cuda.bindings import runtime as cudart
+    for g in graphs:
+        err, = cudart.cudaGraphUpload(g.raw_cuda_graph_exec(), stream.cuda_stream)
+        if int(err) != 0:
+            raise RuntimeError(f"cudaGraphUpload failed: {err}")
+    torch.cuda.synchronize()
+
+
+
 class LayerSet:
     """One independent input set of a round: the layer stack's state, inputs,
     y and status as [L]-leading slabs (`stack`; accept_len [batch] is shared
@@ -278,7 +393,11 @@ def launch_layer(ssm, wl, e):
                           dev_status=e["status"])
 
 
-def run_ours(args, wl, rank, world, local_rank):
+def device_leg(args, wl, rank, world, local_rank):
+    """This rank's share of the timed region on its own GPU: W warm-up
+    steps, then K steps replayed from CUDA graphs between a barrier and a
+    synchronize on each side. Returns this rank's elapsed time and what the
+    summary needs; run_ours takes the maximum over ranks."""
     import ssm_recurrence_verify_b300 as ssm
     from ssm_recurrence_verify_b300 import build as libbuild
     if not os.path.exists(libbuild.LIB):
@@ -324,6 +443,7 @@ def run_ours(args, wl, rank, world, local_rank):
     timed_sets = [(args.warmup + i) % nsets for i in range(K)]
     timed_graphs = capture(timed_sets)
     torch.cuda.synchronize()
+    upload_graphs(warm_graphs + timed_graphs, stream)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -348,26 +468,34 @@ def run_ours(args, wl, rank, world, local_rank):
     for s in sets:
         for e in s.layers:
             assert int(e["status"].item()) == 0, "device reported a bad accept_len"
-    max_ms = max_over_ranks(elapsed_ms, world)
-
     # per-step algorithmic bytes, averaged over the sets the timed steps used
     step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
     used = [step_bytes[si] for si in timed_sets]
-    mean_launch_bytes = statistics.fmean(used) / per_step
-    mean_launch_ms = elapsed_ms / (K * per_step)  # this rank's average launch duration over the timed region
-    achieved = mean_launch_bytes / (mean_launch_ms * 1e-3) / 1e9
+    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 else None
+    return {"elapsed_ms": elapsed_ms, "steps": K, "per_step": per_step, "batch": batch, "nsets": nsets,
+            "launch_bytes": statistics.fmean(used) / per_step, "wall_s": wall1 - wall0, "graphs": len(timed_graphs),
+            "clocks": sampler.summary(wall0, wall1), "e2e": e2e}
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    """The device leg on this rank, then the whole-job figures: the elapsed
+    time is the maximum over ranks, and the value counts every rank's
+    sequences (weak scaling: each rank owns `batch` sequences)."""
+    leg = device_leg(args, wl, rank, world, local_rank)
+    K, per_step, nl = leg["steps"], leg["per_step"], wl.nlayers
+    max_ms = max_over_ranks(leg["elapsed_ms"], world)
+    mean_launch_ms = leg["elapsed_ms"] / (K * per_step)  # this rank's average launch duration over the timed region
+    achieved = leg["launch_bytes"] / (mean_launch_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     # per SSM layer: Bsz K / t_layer, i.e. every rank's sequences x draft tokens x layers per step time
-    tokens_per_step = batch * wl.ntok * world * nl
+    tokens_per_step = leg["batch"] * wl.ntok * world * nl
     value = tokens_per_step * K / (max_ms * 1e-3)
-
-    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 else None
     return {
-        "value": value, "ms_per_step": max_ms / K, "elapsed_ms": max_ms, "wall_s": wall1 - wall0,
-        "launch_ms_mean": mean_launch_ms, "graphs": len(timed_graphs),
-        "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "bytes_per_launch": mean_launch_bytes,
-        "clocks": sampler.summary(wall0, wall1), "nsets": nsets, "e2e": e2e, "launches": K * per_step,
-        "batch": batch, "layers_per_launch": nl // per_step,
+        "value": value, "ms_per_step": max_ms / K, "elapsed_ms": max_ms, "wall_s": leg["wall_s"],
+        "launch_ms_mean": mean_launch_ms, "graphs": leg["graphs"],
+        "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "bytes_per_launch": leg["launch_bytes"],
+        "clocks": leg["clocks"], "nsets": leg["nsets"], "e2e": leg["e2e"], "launches": K * per_step,
+        "batch": leg["batch"], "layers_per_launch": nl // per_step,
     }
 
 
@@ -503,6 +631,7 @@ def run_accept(args, sample: bool, rank, world, local_rank):
     warm = capture([i % nsets for i in range(args.warmup)])
     timed = capture([(args.warmup + i) % nsets for i in range(K)])
     torch.cuda.synchronize()
+    upload_graphs(warm + timed, stream)
     sampler = ClockSampler(local_rank)
     sampler.start()
     with torch.cuda.stream(stream):
@@ -870,14 +999,17 @@ def main(argv=None):
         if not 1 <= args.layers <= wl.nlayers:
             ap.error(f"--layers must be in [1, {wl.nlayers}]")
         wl = dataclasses.replace(wl, nlayers=args.layers, name=f"{wl.name}_first{args.layers}layers")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return launch_ranks(sys.argv[1:] if argv is None else argv, args.gpus)
     rank, world, local_rank = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but the launcher started {world} rank(s)")
 
     if args.impl == "reference":
         return run_reference(args, wl, rank, world)
 
     if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        init_ranks(world, local_rank)
     if args.path != "ssm":
         if args.path == "prefill":
             line = run_prefill(args, rank, world, local_rank)

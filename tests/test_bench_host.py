@@ -170,7 +170,7 @@ def test_reference_arm_line(monkeypatch, capsys):
 def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    assert bench.main(["--impl", "reference", "--workload", "0", "--steps", "3", "--warmup", "3"]) == 0
+    assert bench.main(["--impl", "reference", "--gpus", "2", "--workload", "0", "--steps", "3", "--warmup", "3"]) == 0
     assert capsys.readouterr().out.strip() == ""
 
 
