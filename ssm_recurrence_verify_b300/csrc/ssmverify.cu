@@ -155,7 +155,26 @@ struct Block {
     int tma;      // the first chunk's x / B / C rows may be bulk-copied (16-byte aligned rows)
 };
 
+// Division by a divisor fixed for the launch, as a multiply-high and a shift
+// (the round-up method of Granlund and Montgomery, "Division by invariant
+// integers using multiplication", 1994): with s = ceil(log2 d) and
+// mul = floor(2^32 (2^s - d) / d) + 1, n / d = (mulhi(n, mul) + n) >> s for
+// every 32-bit n, the sum taken in 64 bits. Divisors in [1, 2^31].
+struct FastDiv {
+    uint32_t d, mul, shift;
+};
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    return (uint32_t)(((unsigned long long)__umulhi(n, f.mul) + n) >> f.shift);
+}
+inline FastDiv make_fdiv(uint32_t d) {
+    FastDiv f{d, 0u, 0u};
+    while ((1ull << f.shift) < d) ++f.shift;
+    f.mul = (uint32_t)(((1ull << 32) * ((1ull << f.shift) - d)) / d + 1);
+    return f;
+}
+
 struct Args {
+    FastDiv fd_ptiles, fd_H, fd_bpl, fd_hpg;  // tile decode: P-tiles, heads, sequences per layer, heads per group
     const float *state_in;  // state read by the tile loads
     float *state;           // state written (nullptr for verify)
     const int32_t *slot;    // pool flavours: slot of each sequence (nullptr: sequence b uses slot b)
@@ -376,14 +395,14 @@ template <bool POOL>
 __device__ __forceinline__ Tile decode(const Args &a, long long t, int kRows, int N) {
     Tile T;
     const uint32_t tt = (uint32_t)t;  // the host keeps the tile count below 2^31
-    const int ptile = (int)(tt % (uint32_t)a.ptiles);
-    const uint32_t bh = tt / (uint32_t)a.ptiles;
-    T.h = (int)(bh % (uint32_t)a.H);
-    const uint32_t bb = bh / (uint32_t)a.H;
+    const uint32_t bh = fdiv(tt, a.fd_ptiles);
+    const int ptile = (int)(tt - bh * (uint32_t)a.ptiles);
+    const uint32_t bb = fdiv(bh, a.fd_H);
+    T.h = (int)(bh - bb * (uint32_t)a.H);
     T.b = (long long)bb;
-    T.lay = (int)(bb / (uint32_t)a.bpl);
+    T.lay = (int)fdiv(bb, a.fd_bpl);
     T.bs = (int)(bb - (uint32_t)T.lay * (uint32_t)a.bpl);
-    T.g = T.h / (a.H / a.G);
+    T.g = (int)fdiv((uint32_t)T.h, a.fd_hpg);
     T.row0 = ptile * kRows;
     T.rows = min(kRows, a.P - T.row0);
     long long sb = T.b;
@@ -893,10 +912,9 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         uint32_t dst, bytes;  // dst: offset into the dynamic shared memory; bytes 0: none
         uint32_t total;
     };
-    auto plan = [&](long long tt, int buf) {
+    auto plan = [&](const Tile &T, long long tt, int buf) {
         Plan pl{nullptr, 0u, 0u, 0u};
         if (tt >= a.ntiles) return pl;
-        const Tile T = decode<FL::kPool>(a, tt, ROWS, N);
         const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.bs, a.rep.K), kTC) : 0;
         const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
         const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
@@ -944,7 +962,8 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         fence_proxy_async_smem();
     }
     __syncthreads();
-    issue(plan(t, 0));
+    Tile Tcur = decode<FL::kPool>(a, t, ROWS, N);  // each tile is decoded once, a tile ahead
+    issue(plan(Tcur, t, 0));
 
     // Per-tile scalars and the dt values of the first chunks, loaded one tile
     // ahead (their latency hides behind the previous tile's work).
@@ -953,10 +972,9 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         int jr, jw;  // tokens replayed; verify token after which the state is written (-1: none)
         ChunkDt dR, dV;
     };
-    auto load_in = [&](long long tt) {
+    auto load_in = [&](const Tile &T, long long tt) {
         TileIn in{0.f, 0.f, 0, -1, {0.f, 0.f}, {0.f, 0.f}};
         if (tt >= a.ntiles) return in;
-        const Tile T = decode<FL::kPool>(a, tt, ROWS, N);
         in.Ah = __ldg(a.A + T.lay * a.H + T.h);
         if (FL::kVerifyPhase) in.Dh = __ldg(a.D + T.lay * a.H + T.h);
         if (FL::kReplay) in.jr = accepted(a, T.bs, a.rep.K);
@@ -965,18 +983,21 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         if constexpr (FL::kVerifyPhase) in.dV = load_chunk_dt<Tin, N>(a, a.ver, T, 0, min(a.ver.K, kTC));
         return in;
     };
-    TileIn cur = load_in(t);
+    TileIn cur = load_in(Tcur, t);
 
     uint32_t parity = 0;  // mbarrier phase; raw buffer of the current tile = parity
     while (t < a.ntiles) {
-        const Tile T = decode<FL::kPool>(a, t, ROWS, N);
+        const Tile T = Tcur;
         const float Ah = cur.Ah, Dh = cur.Dh;
         const int jr = cur.jr, jw = cur.jw;
         const int tcR0 = min(jr, kTC), tcV0 = FL::kVerifyPhase ? min(a.ver.K, kTC) : 0;
         const ChunkDt dR = cur.dR, dV = cur.dV;
         const long long tn = next_work<F>(a, t + gridDim.x);
-        const Plan next = plan(tn, (int)(parity ^ 1u));
-        cur = load_in(tn);
+        Tile Tn = T;
+        if (tn < a.ntiles) Tn = decode<FL::kPool>(a, tn, ROWS, N);
+        const Plan next = plan(Tn, tn, (int)(parity ^ 1u));
+        cur = load_in(Tn, tn);
+        Tcur = Tn;
 
         // Wait for the tile's bulk copies; the state tile goes to registers.
         const bool ok = mbar_wait_bounded(&bar, parity);
@@ -2074,6 +2095,10 @@ int run(const ssm_desc_t *d, const Call &c, void *stream, bool dry = false) {
     a.G = d->ngroups;
     a.ptiles = (int)ptiles;
     a.bpl = d->batch;
+    a.fd_ptiles = make_fdiv((uint32_t)ptiles);
+    a.fd_H = make_fdiv((uint32_t)d->nheads);
+    a.fd_bpl = make_fdiv((uint32_t)d->batch);
+    a.fd_hpg = make_fdiv((uint32_t)(d->nheads / d->ngroups));
     a.ntiles = ntiles;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
