@@ -102,7 +102,17 @@ struct Geo {
     static constexpr int kKB = kNCW / 8;                 // mma k-blocks per warp
     static constexpr int kBands = 4 / kWPB;
     static constexpr int kRows = 16 * kBands;            // rows per tile
-    static constexpr int kPad = kNC + 4;                 // padded row of a thread's slots in smem
+    // Padded row of a thread's slots in the staged B / C (floats). With one
+    // warp per band the mma-fragment reads (8-byte loads of lane g*4+tq's row,
+    // 4-byte loads of row tq*4 + g/2) hit 32 distinct banks when the row is
+    // 2 mod 32 floats long; the token-by-token recurrence (two warps per band)
+    // reads 16-byte vectors and needs a multiple of 4.
+    static constexpr int kPad = kWPB == 1 ? kNC + 2 : kNC + 4;
+    // Row strides (floats) of the staged u = dt x and D x, [kTC][stride]: the
+    // loads of u[tq][g] and of D x[2tq + e][g] by the 32 lanes land on
+    // distinct banks with 8 and 4 floats of padding.
+    static constexpr int kUS = kRows + 8;
+    static constexpr int kDS = kRows + 4;
     static_assert(N >= 16 && N <= 256 && (N & (N - 1)) == 0, "dstate must be a power of two in [16, 256]");
 };
 
@@ -133,15 +143,15 @@ struct Lay {
     static constexpr int kRaw = kState + ROWS * N * 4;                  // 2 raw buffers
     static constexpr int kVB = kRaw + 2 * kRawBytes;                    // float, permuted
     static constexpr int kVC = kVB + (V ? BC : 0);                      // float, permuted
-    static constexpr int kVU = kVC + (V ? BC : 0);                      // float [kTC][ROWS]
-    static constexpr int kVDx = kVU + (V ? kTC * ROWS * 4 : 0);         // float [kTC][ROWS]
-    static constexpr int kVAbar = kVDx + (V ? kTC * ROWS * 4 : 0);      // float [kTC]
+    static constexpr int kVU = kVC + (V ? BC : 0);                      // float [kTC][kUS]
+    static constexpr int kVDx = kVU + (V ? kTC * G::kUS * 4 : 0);       // float [kTC][kDS]
+    static constexpr int kVAbar = kVDx + (V ? kTC * G::kDS * 4 : 0);    // float [kTC]
     static constexpr int kVCs = kVAbar + (V ? kTC * 4 : 0);             // float [kTC]
     static constexpr int kVW = kVCs + (V ? kTC * 4 : 0);                // float [kTC]
     static constexpr int kXch = kVW + (V ? kTC * 4 : 0);                // float [bands][32][8] (N = 256)
     static constexpr int kRB = kXch + (V && G::kWPB > 1 ? G::kBands * 32 * 8 * 4 : 0);  // float, permuted
-    static constexpr int kRU = kRB + (R ? BC : 0);                      // float [kTC][ROWS]
-    static constexpr int kRAbar = kRU + (R ? kTC * ROWS * 4 : 0);       // float [kTC]
+    static constexpr int kRU = kRB + (R ? BC : 0);                      // float [kTC][kUS]
+    static constexpr int kRAbar = kRU + (R ? kTC * G::kUS * 4 : 0);     // float [kTC]
     static constexpr int kBytes = kRAbar + (R ? kTC * 4 : 0);
     static_assert(kRawBytes % 16 == 0 && kRaw % 128 == 0, "bulk-copy destinations must be 16-byte aligned");
 };
@@ -269,10 +279,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
-// tf32 high part of x (round to nearest, ties away), as the bit pattern mma reads.
+// tf32 high part of x (rounded toward zero: the top 19 bits), as the bit
+// pattern mma reads. Toward zero is one instruction on sm_103a, where the
+// rounding conversion issues about three and a half.
 __device__ __forceinline__ uint32_t tf32_hi(float x) {
     uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    asm("cvt.rz.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return r;
 }
 
@@ -357,6 +369,18 @@ __device__ __forceinline__ void widen(const Raw8<__nv_bfloat16> &r, float (&v)[8
 
 __device__ __forceinline__ void st4(float *s, float a, float b, float c, float d) {
     *reinterpret_cast<float4 *>(s) = make_float4(a, b, c, d);
+}
+
+// Four consecutive staged B / C slots: one 16-byte store where the padded
+// rows keep 16-byte alignment (Geo::kPad a multiple of 4), else two 8-byte stores.
+template <int N>
+__device__ __forceinline__ void st_slots(float *s, float a, float b, float c, float d) {
+    if constexpr (Geo<N>::kPad % 4 == 0) {
+        st4(s, a, b, c, d);
+    } else {
+        reinterpret_cast<float2 *>(s)[0] = make_float2(a, b);
+        reinterpret_cast<float2 *>(s)[1] = make_float2(c, d);
+    }
 }
 
 // ----------------------------------------------------------------------------- arithmetic (shared by all flavours)
@@ -498,13 +522,13 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
 #pragma unroll
             for (int e = 0; e < 8; ++e) xv[e] = 0.f;
         }
-        float *u = sm<float>(so.U) + t * ROWS + 8 * r8;
+        float *u = sm<float>(so.U) + t * Geo<N>::kUS + 8 * r8;
         st4(u, ssm_input_scale(dtv, xv[0]), ssm_input_scale(dtv, xv[1]), ssm_input_scale(dtv, xv[2]),
             ssm_input_scale(dtv, xv[3]));
         st4(u + 4, ssm_input_scale(dtv, xv[4]), ssm_input_scale(dtv, xv[5]), ssm_input_scale(dtv, xv[6]),
             ssm_input_scale(dtv, xv[7]));
         if (WANT_Y) {
-            float *dx = sm<float>(so.Dx) + t * ROWS + 8 * r8;
+            float *dx = sm<float>(so.Dx) + t * Geo<N>::kDS + 8 * r8;
             st4(dx, __fmul_rn(Dh, xv[0]), __fmul_rn(Dh, xv[1]), __fmul_rn(Dh, xv[2]), __fmul_rn(Dh, xv[3]));
             st4(dx + 4, __fmul_rn(Dh, xv[4]), __fmul_rn(Dh, xv[5]), __fmul_rn(Dh, xv[6]), __fmul_rn(Dh, xv[7]));
         }
@@ -519,8 +543,8 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
         const int tb = t * Geo<N>::kWPB * 4 * Geo<N>::kPad;
         const int p0 = tb + perm_index<N>(8 * n8), p1 = tb + perm_index<N>(8 * n8 + 4);
         if (t >= tc) {
-            st4(sm<float>(so.B) + p0, 0.f, 0.f, 0.f, 0.f);
-            st4(sm<float>(so.B) + p1, 0.f, 0.f, 0.f, 0.f);
+            st_slots<N>(sm<float>(so.B) + p0, 0.f, 0.f, 0.f, 0.f);
+            st_slots<N>(sm<float>(so.B) + p1, 0.f, 0.f, 0.f, 0.f);
             continue;
         }
         Raw8<Tin> r;
@@ -528,14 +552,14 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
         if (FROM_RAW) lds8(sm<const Tin>(rawB) + t * N + 8 * n8, r);
         else ld8(Bp + off, blk.vec_bc, 8, r);
         widen(r, v);
-        st4(sm<float>(so.B) + p0, v[0], v[1], v[2], v[3]);
-        st4(sm<float>(so.B) + p1, v[4], v[5], v[6], v[7]);
+        st_slots<N>(sm<float>(so.B) + p0, v[0], v[1], v[2], v[3]);
+        st_slots<N>(sm<float>(so.B) + p1, v[4], v[5], v[6], v[7]);
         if (WANT_Y) {
             if (FROM_RAW) lds8(sm<const Tin>(rawC) + t * N + 8 * n8, r);
             else ld8(Cp + off, blk.vec_bc, 8, r);
             widen(r, v);
-            st4(sm<float>(so.C) + p0, v[0], v[1], v[2], v[3]);
-            st4(sm<float>(so.C) + p1, v[4], v[5], v[6], v[7]);
+            st_slots<N>(sm<float>(so.C) + p0, v[0], v[1], v[2], v[3]);
+            st_slots<N>(sm<float>(so.C) + p1, v[4], v[5], v[6], v[7]);
         }
     }
     // Per token (the last warp, whose lanes carry no tile-copy work): Abar and,
@@ -623,7 +647,7 @@ __device__ __forceinline__ void recur_token(float2 (&hs)[2][Geo<N>::kNC / 2], co
     constexpr int ROWS = G::kRows;
     const float abar = sm<const float>(so.Abar)[t];
     const float2 ab2 = make_float2(abar, abar);
-    const float *urow = sm<const float>(so.U) + t * ROWS + L.band * 16 + L.g;
+    const float *urow = sm<const float>(so.U) + t * G::kUS + L.band * 16 + L.g;
     const float2 u0 = make_float2(urow[0], urow[0]);
     const float2 u1 = make_float2(urow[8], urow[8]);
     const float *bs = sm<const float>(so.B) + (t * G::kWPB * 4 + L.half * 4 + L.tq) * G::kPad;
@@ -638,8 +662,10 @@ __device__ __forceinline__ void recur_token(float2 (&hs)[2][Geo<N>::kNC / 2], co
     }
 }
 
-// The split of an fp32 operand for mma: exact inputs (bf16 values) need only
-// the high part.
+// The split of an fp32 operand for mma: x = hi + lo exactly in fp32, hi the
+// tf32 truncation of x, |lo| < 2^-10 |x|; mma reads lo to tf32 precision, so
+// the two products carry |error| < 2^-20 |x| per term. Exact inputs (bf16
+// values) need only the high part.
 struct Split {
     uint32_t hi, lo;
 };
@@ -675,11 +701,11 @@ __device__ __forceinline__ AdvW adv_weights(const float *abar, int tq, int tc) {
 struct AFrag {
     Split a0, a1, a2, a3;
 };
-template <int ROWS>
+template <int US>
 __device__ __forceinline__ AFrag adv_frag(const float *U, const Lane &L, const AdvW &w) {
     const int r0 = L.band * 16 + L.g, r1 = r0 + 8, t0 = L.tq, t1 = L.tq + 4;
-    return AFrag{split(__fmul_rn(w.w0, U[t0 * ROWS + r0])), split(__fmul_rn(w.w0, U[t0 * ROWS + r1])),
-                 split(__fmul_rn(w.w1, U[t1 * ROWS + r0])), split(__fmul_rn(w.w1, U[t1 * ROWS + r1]))};
+    return AFrag{split(__fmul_rn(w.w0, U[t0 * US + r0])), split(__fmul_rn(w.w0, U[t0 * US + r1])),
+                 split(__fmul_rn(w.w1, U[t1 * US + r0])), split(__fmul_rn(w.w1, U[t1 * US + r1]))};
 }
 
 // The rank-tc term of one n-block, sum_s w_s u_s B_s^T, from zero (small
@@ -711,7 +737,7 @@ __device__ __forceinline__ void advance_mma(float2 (&hs)[2][Geo<N>::kNC / 2], co
     using G = Geo<N>;
     static_assert(G::kWPB == 1, "one warp per band");
     const AdvW w = adv_weights(sm<const float>(so.Abar), L.tq, tc);
-    const AFrag a = adv_frag<G::kRows>(sm<const float>(so.U), L, w);
+    const AFrag a = adv_frag<G::kUS>(sm<const float>(so.U), L, w);
     const float2 l2 = make_float2(w.lam, w.lam);
     const float *Bs = sm<const float>(so.B) + (L.g >> 1) * G::kPad + (L.g & 1);
     const float *b0p = Bs + L.tq * 4 * G::kPad, *b1p = Bs + (L.tq + 4) * 4 * G::kPad;
@@ -734,7 +760,7 @@ __device__ __forceinline__ void commit_mma(const float2 (&hs)[2][Geo<N>::kNC / 2
     using G = Geo<N>;
     static_assert(G::kWPB == 1, "one warp per band");
     const AdvW w = adv_weights(sm<const float>(so.Abar), L.tq, jc);
-    const AFrag a = adv_frag<G::kRows>(sm<const float>(so.U), L, w);
+    const AFrag a = adv_frag<G::kUS>(sm<const float>(so.U), L, w);
     const float2 l2 = make_float2(w.lam, w.lam);
     const float *Bs = sm<const float>(so.B) + (L.g >> 1) * G::kPad + (L.g & 1);
     const float *b0p = Bs + L.tq * 4 * G::kPad, *b1p = Bs + (L.tq + 4) * 4 * G::kPad;
@@ -825,8 +851,8 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
     const float z0 = __shfl_sync(0xffffffffu, w2[0], src1), z1 = __shfl_sync(0xffffffffu, w2[1], src1);
     const Split wb0 = split((L.tq & 1) ? x1 : x0), wb1 = split((L.tq & 1) ? z1 : z0);
     const float *U = sm<const float>(so.U) + L.band * 16 + L.g;
-    const Split ua0 = split(U[L.tq * ROWS]), ua1 = split(U[L.tq * ROWS + 8]), ua2 = split(U[(L.tq + 4) * ROWS]),
-                ua3 = split(U[(L.tq + 4) * ROWS + 8]);
+    const Split ua0 = split(U[L.tq * G::kUS]), ua1 = split(U[L.tq * G::kUS + 8]),
+                ua2 = split(U[(L.tq + 4) * G::kUS]), ua3 = split(U[(L.tq + 4) * G::kUS + 8]);
     // y = w (.) Y0 + U W^T
     const float *wt = sm<const float>(so.W);
     float d[4];
@@ -842,7 +868,7 @@ __device__ __forceinline__ void chunk_y(const float2 (&hs)[2][Geo<N>::kNC / 2], 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int t = 2 * L.tq + (i & 1), r = L.band * 16 + L.g + 8 * (i >> 1);
-        if (t < tc && r < rows) __stcs(ychunk + t * ystride + r, d[i] + Dx[t * ROWS + r]);
+        if (t < tc && r < rows) __stcs(ychunk + t * ystride + r, d[i] + Dx[t * G::kDS + r]);
     }
 }
 
