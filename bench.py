@@ -722,10 +722,12 @@ def run_prefill(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     H, P, N, G = PREFILL_SHAPES[args.prefill_shape]
-    wl = synth.custom_workload(1, H, P, N, G, 2048, synth.BF16, seed=500, accept="all")
+    in_dtype = synth.BF16 if args.prefill_dtype == "bf16" else synth.F32
+    wl = synth.custom_workload(1, H, P, N, G, 2048, in_dtype, seed=500, accept="all")
     T = wl.ntok
     # inputs + y + state of one step; the workspace (shared) adds its own traffic
-    step_bytes = T * (wl.nheads * wl.headdim * (2 + 4) + 2 * wl.ngroups * wl.dstate * 2 + wl.nheads * 2) \
+    eb = wl.in_elem_bytes()
+    step_bytes = T * (wl.nheads * wl.headdim * (eb + 4) + 2 * wl.ngroups * wl.dstate * eb + wl.nheads * eb) \
         + 2 * wl.nheads * wl.headdim * wl.dstate * 4
     nsets = max(2, math.ceil(2 * L2_BYTES / step_bytes) + 1)  # each set read again after > 2x the L2 of others
     sets = []
@@ -782,8 +784,9 @@ def run_prefill(args, rank, world, local_rank):
         "metric": PREFILL_METRIC, "value": T * world / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": 3, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": f"prefill_{args.prefill_shape}_layer_b1_t{T}_h{H}_p{P}_n{N}_g{G}", "prompt_tokens": T,
-                   "batch_per_gpu": 1, "in_dtype": "bf16", "workspace_bytes": nbytes,
+        "config": {"workload": f"prefill_{args.prefill_shape}_layer_b1_t{T}_h{H}_p{P}_n{N}_g{G}"
+                               + ("" if args.prefill_dtype == "bf16" else "_f32"), "prompt_tokens": T,
+                   "batch_per_gpu": 1, "in_dtype": args.prefill_dtype, "workspace_bytes": nbytes,
                    "timing": f"{steps} launches captured in one CUDA graph",
                    "l2": f"{nsets} independent input sets rotated (each read again after > 2x the L2 of other traffic)"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
@@ -989,6 +992,9 @@ def main(argv=None):
     ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill"], default="ssm",
                     help="ssm: the verify/commit step (default); accept_*: the acceptance step alone; "
                          "prefill: a 2048-token prompt through one layer")
+    ap.add_argument("--prefill-dtype", choices=["bf16", "f32"], default="bf16",
+                    help="prompt input dtype of --path prefill (f32 prompts take the mma.sync chunk-state pass and "
+                         "the tile kernel's chunk outputs instead of the tcgen05 passes)")
     ap.add_argument("--prefill-shape", choices=sorted(PREFILL_SHAPES), default="llama3_8b",
                     help="layer shape of --path prefill")
     args = ap.parse_args(argv)
