@@ -696,9 +696,53 @@ def run_accept(args, sample: bool, rank, world, local_rank):
 
 # ----------------------------------------------------------------------------- prefill
 
-PREFILL_METRIC = "prompt tokens/s per SSM layer (prefill); achieved FP32 TFLOP/s vs B300 peak"
-SM_COUNT, FP32_LANES, SM_MAX_GHZ = 148, 128, 2.032  # B300: the FP32 peak is derived from these
-FP32_PEAK_TFLOPS = SM_COUNT * FP32_LANES * 2 * SM_MAX_GHZ / 1e3
+PREFILL_METRIC = "prompt tokens/s per SSM layer (prefill); achieved tensor TFLOP/s vs B300 peak"
+FALLBACK_BF16_TFLOPS = 1800.0
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tensor rates of B300: tf32 1.1, bf16 2.25 PFLOP/s
+
+
+def bf16_peak():
+    """Measured dense bf16 tensor throughput (cuBLAS burst) of the B300s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_tensor_macs(H: int, P: int, N: int, T: int, L: int, bf16: bool):
+    """Multiply-adds the chunked prefill issues on the tensor cores for one
+    prompt of T tokens in chunks of L, split products counted as issued.
+    Returns (MACs, operand kind), or (None, why) for shapes not modelled.
+
+    bf16, N 128, L 128, P a multiple of 64: the tcgen05 passes. Chunk states
+    S = (w o U) B with w o U in two bf16 parts (B exact): 2 H P T N. Chunk
+    outputs per tile of PR rows (128, or 64 where P is not a multiple of 128):
+    G = C B^T (L L N), Yi = C H0^T with H0 in two parts (2 L N PR), Yc = M X
+    with M in two parts (2 L L PR).
+    Otherwise (mma.sync m16n8k8 tf32, 1024 MACs each): chunk states with w o U
+    split, fp32 B split too (2 or 3 products); chunk outputs by the tile
+    kernel in 8-token sub-chunks, per warp (16 rows) and sub-chunk: h C^T over
+    N / 8 k-blocks (2 or 3 products), the Gram C B^T likewise (1 or 3, every
+    warp), the intra-chunk term (3), and the state advance over N / 8 blocks
+    (2 or 3) for every sub-chunk but a chunk's last."""
+    nch = T // L
+    if bf16 and N == 128 and L == 128 and P % 64 == 0:
+        pr = 128 if P % 128 == 0 else 64
+        states = 2 * H * P * T * N
+        outputs = nch * H * (P // pr) * (L * L * N + 2 * L * N * pr + 2 * L * L * pr)
+        return states + outputs, "tcgen05 kind::f16 (bf16 operands, fp32 accumulation)"
+    if N > 128:
+        return None, "not modelled for dstate > 128"
+    sp = 2 if bf16 else 3
+    states = sp * H * P * T * N
+    warps = nch * H * (-(-P // 16))  # 16-row bands of the 64-row tiles
+    sub = L // 8
+    per_sub = (N // 8) * sp + (N // 8) * (1 if bf16 else 3) + 3
+    adv = (N // 8) * sp
+    outputs = warps * (sub * per_sub + (sub - 1) * adv) * 1024
+    return states + outputs, "mma.sync m16n8k8 tf32 (fp32 accumulation)"
 
 
 # prompt shapes of the prefill bench: name -> (heads, headdim, dstate, ngroups)
@@ -777,9 +821,18 @@ def run_prefill(args, rank, world, local_rank):
     ms_one_pass = timed(False, max(3, steps // 4))
     assert int(status.item()) == 0, "device reported a problem"
     ms_max = max_over_ranks(ms, world)
-    flops = 5.0 * T * wl.nheads * wl.headdim * wl.dstate
-    achieved = flops / (ms * 1e-3) / 1e12
+    # chunk length the library chose: the workspace holds one state per chunk (+ a small slot map)
+    nch = nbytes // (wl.nheads * wl.headdim * wl.dstate * 4) if nbytes > 0 else 0
+    L = T // nch if nch > 0 else T
+    bf16 = args.prefill_dtype == "bf16"
+    macs, kind = prefill_tensor_macs(H, P, N, T, L, bf16) if nch > 0 else (None, "one pass")
+    peak, peak_kind = bf16_peak()
+    if not bf16:
+        peak *= TF32_PER_BF16
+    achieved = 2.0 * macs / (ms * 1e-3) / 1e12 if macs else None
     io_bytes = step_bytes
+    hbm, hbm_kind = hbm_peak()
+    io_gbs = io_bytes / (ms * 1e-3) / 1e9
     return {
         "metric": PREFILL_METRIC, "value": T * world / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": 3, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -789,11 +842,16 @@ def run_prefill(args, rank, world, local_rank):
                    "batch_per_gpu": 1, "in_dtype": args.prefill_dtype, "workspace_bytes": nbytes,
                    "timing": f"{steps} launches captured in one CUDA graph",
                    "l2": f"{nsets} independent input sets rotated (each read again after > 2x the L2 of other traffic)"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
-                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 flops x 2.032 GHz",
-                     "algorithmic_flops_per_step": flops,
-                     "hbm_gbs_on_io_bytes": io_bytes / (ms * 1e-3) / 1e9},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "peak_source": (f"{peak_kind} bf16 dense (MEASURED_PEAKS.json bf16_tflops)" if bf16 else
+                                     f"{peak_kind} bf16 dense x {TF32_PER_BF16:.3f} (nominal tf32 / bf16 ratio)"),
+                     "work": f"tensor-core multiply-adds issued by the chunked form ({kind}; chunk length {L}), "
+                             "split products counted as issued, x 2 flops, over the whole step (three kernels)",
+                     "issued_flops_per_step": 2.0 * macs if macs else None,
+                     "hbm_gbs_on_io_bytes": io_gbs, "hbm_frac_on_io_bytes": io_gbs / hbm,
+                     "io_bytes_per_step": io_bytes,
+                     "io_bytes": "prompt inputs read once, y written once in fp32, the cached state read and written"},
         "one_pass_ms": ms_one_pass,
         # the chunked form is three kernels per prompt (chunk states, scan, outputs); the one pass is one
         "gpu_launches": steps * (3 if nbytes > 0 else 1), "clocks": sampler.summary(wall0, wall1),

@@ -183,3 +183,16 @@ def test_cgroup_cpu_limit(tmp_path):
     f.write_text("max 100000\n")
     assert bench.cgroup_cpu_limit(str(f)) is None
     assert bench.cgroup_cpu_limit(str(tmp_path / "absent")) is None
+
+
+def test_prefill_tensor_work_by_hand():
+    """Issued tensor-core multiply-adds of a 2048-token Llama-3-8B-layer prompt
+    (H 32, P N L 128, bf16): chunk states 2 H P T N = 2^31; chunk outputs, per
+    chunk and head, G (128^3) + Yi in two parts (2 x 128^3) + Yc in two parts
+    (2 x 128^3) = 5 x 2^21, over 16 chunks x 32 heads = 5 x 2^30."""
+    macs, kind = bench.prefill_tensor_macs(32, 128, 128, 2048, 128, True)
+    assert macs == 2 ** 31 + 5 * 2 ** 30 and kind.startswith("tcgen05")
+    # 64-row output tiles (P 64): G once per tile, the row products at 64 rows
+    macs64, _ = bench.prefill_tensor_macs(2, 64, 128, 256, 128, True)
+    assert macs64 == 2 * 2 * 64 * 256 * 128 + 2 * 2 * (128 ** 3 + 2 * 128 * 128 * 64 + 2 * 128 * 128 * 64)
+    assert bench.prefill_tensor_macs(1, 64, 256, 256, 128, False)[0] is None
