@@ -139,6 +139,39 @@ def algorithmic_bytes(wl: synth.Workload, batch: int, accepted_nonzero: int) -> 
             + batch * K * H * P * 4 + (0 if wl.accept == "all" else batch * 4))
 
 
+def tile_tensor_macs(wl: synth.Workload, accept_len, layers: int) -> int:
+    """Multiply-adds one fused verify+commit launch issues on the tensor cores
+    (mma.sync m16n8k8 tf32, 1024 each), at N <= 128 (one warp per 16-row band):
+    per warp and 8-token chunk, y = h C^T over N / 8 k-blocks (2 products for
+    bf16 inputs, 3 for fp32), the Gram C B^T (1 or 3) and the intra-chunk term
+    (3); per state update (N / 8 n-blocks, 2 or 3 products) as the kernel
+    takes them: through a chunk that more chunks follow, plus the committed
+    state inside it when j falls there, and up to j in the last chunk."""
+    H, P, N, K = wl.nheads, wl.headdim, wl.dstate, wl.ntok
+    if N > 128:
+        return 0
+    bf16 = wl.in_dtype != synth.F32
+    py, pg, pa = (2, 1, 2) if bf16 else (3, 3, 3)
+    warps = -(-P // 16)  # 16-row bands per (sequence, head)
+    per_y = (N // 8) * py + (N // 8) * pg + 3
+    per_upd = (N // 8) * pa
+    total = 0
+    for j in accept_len:
+        j = int(j) if wl.accept != "all" else K
+        mma = 0
+        for t0 in range(0, K, 8):
+            tc = min(8, K - t0)
+            mma += per_y
+            more = t0 + tc < K
+            jc = j - t0 if 0 < j - t0 <= tc else 0  # committed state after token jc - 1 of this chunk
+            if more:
+                mma += per_upd * (2 if 0 < jc < tc else 1)
+            elif jc > 0:
+                mma += per_upd
+        total += mma
+    return total * H * warps * layers * 1024
+
+
 # ----------------------------------------------------------------------------- clocks
 
 def physical_gpu(local_rank: int) -> str:
@@ -471,9 +504,12 @@ def device_leg(args, wl, rank, world, local_rank):
     # per-step algorithmic bytes, averaged over the sets the timed steps used
     step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
     used = [step_bytes[si] for si in timed_sets]
+    step_macs = [tile_tensor_macs(wl, s.layers[0]["host"]["accept_len"], nl) for s in sets]
     e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 else None
     return {"elapsed_ms": elapsed_ms, "steps": K, "per_step": per_step, "batch": batch, "nsets": nsets,
-            "launch_bytes": statistics.fmean(used) / per_step, "wall_s": wall1 - wall0, "graphs": len(timed_graphs),
+            "launch_bytes": statistics.fmean(used) / per_step,
+            "launch_macs": statistics.fmean(step_macs[si] for si in timed_sets) / per_step,
+            "wall_s": wall1 - wall0, "graphs": len(timed_graphs),
             "clocks": sampler.summary(wall0, wall1), "e2e": e2e}
 
 
@@ -494,6 +530,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "value": value, "ms_per_step": max_ms / K, "elapsed_ms": max_ms, "wall_s": leg["wall_s"],
         "launch_ms_mean": mean_launch_ms, "graphs": leg["graphs"],
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "bytes_per_launch": leg["launch_bytes"],
+        "macs_per_launch": leg.get("launch_macs", 0),
         "clocks": leg["clocks"], "nsets": leg["nsets"], "e2e": leg["e2e"], "launches": K * per_step,
         "batch": leg["batch"], "layers_per_launch": nl // per_step,
     }
@@ -1018,6 +1055,23 @@ def run_reference(args, wl, rank, world):
     return 0
 
 
+def tensor_line(r, wl):
+    """The tensor-pipe side of the roofline (the HBM side is `roofline`): the
+    mma.sync tf32 work one launch issues, per its average duration, against
+    the tf32 dense peak (the measured bf16 peak x the nominal tf32 / bf16
+    ratio). At K = 16 the path sits near the compute / HBM ridge."""
+    macs = r.get("macs_per_launch", 0)
+    if not macs:
+        return None
+    bf, kind = bf16_peak()
+    peak = bf * TF32_PER_BF16
+    achieved = 2.0 * macs / (r["launch_ms_mean"] * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "issued_flops_per_launch": 2.0 * macs,
+            "work": "mma.sync m16n8k8 tf32 multiply-adds issued (split products counted), x 2 flops",
+            "peak_source": f"{kind} bf16 dense x {TF32_PER_BF16:.3f} (nominal tf32 / bf16 ratio)"}
+
+
 def workload_config(wl, nsets):
     cfg = {"workload": wl.name, "batch_per_gpu": wl.batch, "layers": wl.nlayers, "nheads": wl.nheads,
            "headdim": wl.headdim, "dstate": wl.dstate, "ngroups": wl.ngroups, "draft_tokens": wl.ntok,
@@ -1111,6 +1165,7 @@ def main(argv=None):
                          "algorithmic_bytes_per_launch": r["bytes_per_launch"],
                          "launch_us_mean": r["launch_ms_mean"] * 1e3,
                          "frac_of_8tbs_spec": r["achieved_gbs"] / HBM_SPEC_GBS},
+            "tensor": tensor_line(r, wl),
             "cpu_baseline": cpu,
             "cpu_baseline_threads": cpu_all,
             "e2e": r["e2e"],

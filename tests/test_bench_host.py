@@ -196,3 +196,16 @@ def test_prefill_tensor_work_by_hand():
     macs64, _ = bench.prefill_tensor_macs(2, 64, 128, 256, 128, True)
     assert macs64 == 2 * 2 * 64 * 256 * 128 + 2 * 2 * (128 ** 3 + 2 * 128 * 128 * 64 + 2 * 128 * 128 * 64)
     assert bench.prefill_tensor_macs(1, 64, 256, 256, 128, False)[0] is None
+
+
+def test_tile_tensor_work_by_hand():
+    """mma.sync work of one launch, K 16 (two 8-token chunks), N 128, bf16, one
+    16-row band: y per chunk 16 x 2 + 16 x 1 + 3 = 51 mma, a state update 16 x 2
+    = 32. j = 0: y, y and the advance through chunk 0 (134); j = 5: the
+    committed state inside chunk 0 and the advance past it (166); j = 12 and
+    j = 16: the advance through chunk 0 and the update up to j in chunk 1 (166)."""
+    wl = synth.custom_workload(4, 1, 16, 128, 1, 16, synth.BF16, seed=3)
+    assert bench.tile_tensor_macs(wl, [0, 5, 12, 16], 1) == (134 + 166 + 166 + 166) * 1024
+    assert bench.tile_tensor_macs(wl, [0], 3) == 3 * 134 * 1024  # layers multiply
+    f32 = synth.custom_workload(1, 1, 16, 128, 1, 8, synth.F32, seed=3)
+    assert bench.tile_tensor_macs(f32, [8], 1) == (16 * 3 + 16 * 3 + 3 + 16 * 3) * 1024
