@@ -33,13 +33,14 @@ class HostPipeline:
     are device ``[H]`` float32. Inputs given to :meth:`run` are host tensors
     with the layouts of ``ssmverify`` (pinned memory for asynchronous copies).
     ``chunks`` sequence chunks are processed per call; ``slots`` device staging
-    slots rotate between them. ``streams`` (copy-in, kernel, copy-out) may be
-    shared by the pipelines of several layers; each pipeline orders only its
-    own slots.
+    slots (default: twice the chunks, so that the next chunks' copies need not
+    wait for earlier read-backs) rotate between them. ``streams`` (copy-in,
+    kernel, copy-out) may be shared by the pipelines of several layers; each
+    pipeline orders only its own slots.
     """
 
     def __init__(self, state: torch.Tensor, A: torch.Tensor, D: torch.Tensor, ntok: int, ngroups: int,
-                 in_dtype: torch.dtype = torch.bfloat16, chunks: int = 2, slots: int = 3, streams=None):
+                 in_dtype: torch.dtype = torch.bfloat16, chunks: int = 4, slots: Optional[int] = None, streams=None):
         if not state.is_cuda:
             raise ValueError("state must be a CUDA tensor")
         self.state, self.A, self.D = state, A, D
@@ -49,7 +50,7 @@ class HostPipeline:
         self.chunks = max(1, min(chunks, bsz))
         self.bounds = [(bsz * i) // self.chunks for i in range(self.chunks + 1)]
         cmax = max(self.bounds[i + 1] - self.bounds[i] for i in range(self.chunks))
-        self.nslots = max(1, slots)
+        self.nslots = max(1, 2 * self.chunks if slots is None else slots)
 
         def dev(*shape, dtype=in_dtype):
             return torch.empty(shape, dtype=dtype, device=self.dev)
