@@ -543,9 +543,9 @@ def run_e2e(ssm, args, wl, s, stream, dev, world):
     kernel of another and the read-back of a third, across all layers."""
     from ssm_recurrence_verify_b300.hostpipe import HostPipeline
     streams = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
-    # 4 sequence chunks with twice as many staging slots measured best on the serving workload
-    # (2 chunks with 3 slots: 3-12 % slower; odd chunk counts slower still)
-    chunks = min(4, s.layers[0]["x"].shape[0])
+    # 2 sequence chunks and 4 staging slots taken in turn measured best on the serving workload
+    # (2 slots: 11 % slower; 4 chunks with 8 slots: 6 % slower)
+    chunks = min(2, s.layers[0]["x"].shape[0])
     pipes, host = [], []
     for e in s.layers:
         pipes.append(HostPipeline(e["state0"], e["A"], e["D"], wl.ntok, wl.ngroups, wl.torch_in_dtype,

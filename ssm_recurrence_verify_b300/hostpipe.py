@@ -40,7 +40,7 @@ class HostPipeline:
     """
 
     def __init__(self, state: torch.Tensor, A: torch.Tensor, D: torch.Tensor, ntok: int, ngroups: int,
-                 in_dtype: torch.dtype = torch.bfloat16, chunks: int = 4, slots: Optional[int] = None, streams=None):
+                 in_dtype: torch.dtype = torch.bfloat16, chunks: int = 2, slots: Optional[int] = None, streams=None):
         if not state.is_cuda:
             raise ValueError("state must be a CUDA tensor")
         self.state, self.A, self.D = state, A, D
@@ -67,6 +67,9 @@ class HostPipeline:
         self.s_in, self.s_k, self.s_out = streams
         # slot free again once its y has been copied out
         self.freed: List[Optional[torch.cuda.Event]] = [None] * self.nslots
+        # slots are taken in turn across calls, so that with more slots than chunks a call's
+        # copies in need not wait for the previous call's read-backs from the same slots
+        self.next_slot = 0
 
     def _h2d(self, dst: torch.Tensor, src: torch.Tensor) -> None:
         """Host -> device on the copy-in stream: page-locked sources are read
@@ -87,7 +90,8 @@ class HostPipeline:
             n = hi - lo
             if n == 0:
                 continue
-            k = c % self.nslots
+            k = self.next_slot
+            self.next_slot = (self.next_slot + 1) % self.nslots
             with torch.cuda.stream(self.s_in):
                 if self.freed[k] is not None:
                     self.s_in.wait_event(self.freed[k])
@@ -135,6 +139,7 @@ def capture_step(pipelines, inputs, device=None, repeat: int = 1) -> torch.cuda.
     cap = torch.cuda.Stream(device=device)
     for p in pipelines:
         p.freed = [None] * p.nslots
+        p.next_slot = 0
     with torch.cuda.graph(g, stream=cap):
         fork = torch.cuda.Event()
         fork.record(cap)
@@ -149,4 +154,5 @@ def capture_step(pipelines, inputs, device=None, repeat: int = 1) -> torch.cuda.
             cap.wait_event(e)
     for p in pipelines:
         p.freed = [None] * p.nslots
+        p.next_slot = 0
     return g
