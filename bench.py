@@ -590,6 +590,100 @@ def run_e2e(ssm, args, wl, s, stream, dev, world):
                     f"CUDA graph"}
 
 
+def run_e2e_pieces(args, local_rank):
+    """The end-to-end step of the serving workload taken apart: each piece of
+    one HostPipeline step (2 sequence chunks, 4 staging slots) enqueued as the
+    pipeline does it, captured into a CUDA graph of 16 steps and timed per
+    step: the SM pulls of the inputs, the copy-engine read-back of y, both at
+    once, the chunk kernels, pulls and kernels at once, and the whole step."""
+    import ssm_recurrence_verify_b300 as ssm
+    from ssm_recurrence_verify_b300 import build as libbuild
+    from ssm_recurrence_verify_b300 import ssmverify as sv
+    from ssm_recurrence_verify_b300.hostpipe import HostPipeline, capture_step
+    if not os.path.exists(libbuild.LIB):
+        libbuild.build()
+    ssm.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    e = LayerSet(wl, wl.batch, 0, 0, dev, 1).layers[0]
+    h = {k: e["host"][k].pin_memory() for k in ("x", "B", "C", "dt", "accept_len")}
+    h["y"] = torch.empty(e["y"].shape, dtype=torch.float32).pin_memory()
+    streams = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
+    p = HostPipeline(e["state0"], e["A"], e["D"], wl.ntok, wl.ngroups, wl.torch_in_dtype, chunks=2, streams=streams)
+    rep = E2E_STEPS_PER_GRAPH
+    reps = max(2, args.steps // rep)
+
+    def chunks():
+        for c in range(p.chunks):
+            lo, hi = p.bounds[c], p.bounds[c + 1]
+            yield c, lo, hi, hi - lo
+
+    def pulls():
+        for c, lo, hi, n in chunks():
+            sv.copy_from_host_n(((p.slot_x[c][:n], h["x"][lo:hi]), (p.slot_B[c][:n], h["B"][lo:hi]),
+                                 (p.slot_C[c][:n], h["C"][lo:hi]), (p.slot_dt[c][:n], h["dt"][lo:hi]),
+                                 (p.slot_acc[c][:n], h["accept_len"][lo:hi])), stream=p.s_in)
+
+    def readback():
+        with torch.cuda.stream(p.s_out):
+            for c, lo, hi, n in chunks():
+                h["y"][lo:hi].copy_(p.slot_y[c][:n], non_blocking=True)
+
+    def kernels():
+        for c, lo, hi, n in chunks():
+            sv.verify_commit(p.state[lo:hi], p.slot_x[c][:n], p.slot_B[c][:n], p.slot_C[c][:n], p.slot_dt[c][:n],
+                             p.A, p.D, p.slot_acc[c][:n], y=p.slot_y[c][:n], dev_status=p.status, stream=p.s_k)
+
+    def time_graph(fn):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        with torch.cuda.graph(g, stream=cap):
+            fork = torch.cuda.Event()
+            fork.record(cap)
+            for st in streams:
+                st.wait_event(fork)
+            for _ in range(rep):
+                fn()
+            for st in streams:
+                ev = torch.cuda.Event()
+                ev.record(st)
+                cap.wait_event(ev)
+        return g
+
+    args_ = (h["x"], h["B"], h["C"], h["dt"], h["accept_len"], h["y"])
+    pulls(), readback(), kernels(), p.run(*args_)
+    torch.cuda.synchronize()
+    graphs = {"pull_us": time_graph(pulls), "readback_us": time_graph(readback),
+              "pull_and_readback_us": time_graph(lambda: (pulls(), readback())),
+              "kernels_us": time_graph(kernels), "pull_and_kernels_us": time_graph(lambda: (pulls(), kernels())),
+              "step_us": capture_step([p], [args_], dev, repeat=rep)}
+    upload_graphs(list(graphs.values()), torch.cuda.current_stream(dev))
+    rs = torch.cuda.Stream(device=dev)
+    out = {}
+    for name, g in graphs.items():
+        with torch.cuda.stream(rs):
+            for _ in range(2):
+                g.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(rs):
+            t0.record(rs)
+            for _ in range(reps):
+                g.replay()
+            t1.record(rs)
+        torch.cuda.synchronize()
+        out[name] = t0.elapsed_time(t1) * 1e3 / (reps * rep)
+    assert int(p.status.item()) == 0, "device reported a bad accept_len"
+    bytes_in = sum(t.numel() * t.element_size() for k, t in h.items() if k != "y")
+    bytes_out = h["y"].numel() * 4
+    return {"path": "e2e_pieces", "workload": wl.name, "steps_per_graph": rep, "graphs_timed": reps,
+            "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
+            **{k: round(v, 1) for k, v in out.items()},
+            "step_tokens_per_s": wl.batch * wl.ntok / (out["step_us"] * 1e-6),
+            "transfer_bound_tokens_per_s": wl.batch * wl.ntok / (out["pull_and_readback_us"] * 1e-6)}
+
+
 # ----------------------------------------------------------------------------- acceptance step
 
 ACCEPT_METRIC = "draft tokens decided/s (acceptance step); achieved HBM GB/s vs B300 peak"
@@ -1104,9 +1198,10 @@ def main(argv=None):
                     help="run only the first N layers of a layer stack (a smaller case for profiling)")
     ap.add_argument("--per-layer-launches", action="store_true",
                     help="run a layer stack as one launch per layer instead of one launch over all layers")
-    ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill"], default="ssm",
+    ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill", "e2e_pieces"], default="ssm",
                     help="ssm: the verify/commit step (default); accept_*: the acceptance step alone; "
-                         "prefill: a 2048-token prompt through one layer")
+                         "prefill: a 2048-token prompt through one layer; e2e_pieces: the host-buffer step of the "
+                         "workload taken apart (copies in, read-back, kernels, each alone and together)")
     ap.add_argument("--prefill-dtype", choices=["bf16", "f32"], default="bf16",
                     help="prompt input dtype of --path prefill (f32 prompts take the mma.sync chunk-state pass and "
                          "the tile kernel's chunk outputs instead of the tcgen05 passes)")
@@ -1134,6 +1229,8 @@ def main(argv=None):
     if args.path != "ssm":
         if args.path == "prefill":
             line = run_prefill(args, rank, world, local_rank)
+        elif args.path == "e2e_pieces":
+            line = run_e2e_pieces(args, local_rank)
         else:
             line = run_accept(args, args.path == "accept_sample", rank, world, local_rank)
         if rank == 0:
