@@ -1144,7 +1144,7 @@ def run_reference(args, wl, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
-        "config": workload_config(wl, None),
+        "config": workload_config(wl, None, world),
         "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": 1, "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -1169,10 +1169,12 @@ def tensor_line(r, wl):
             "peak_source": f"{kind} bf16 dense x {TF32_PER_BF16:.3f} (nominal tf32 / bf16 ratio)"}
 
 
-def workload_config(wl, nsets):
+def workload_config(wl, nsets, world: int = 1):
     cfg = {"workload": wl.name, "batch_per_gpu": wl.batch, "layers": wl.nlayers, "nheads": wl.nheads,
            "headdim": wl.headdim, "dstate": wl.dstate, "ngroups": wl.ngroups, "draft_tokens": wl.ntok,
-           "in_dtype": wl.in_dtype, "state_dtype": "f32", "accept_len": wl.accept, "parallelism": "replicas"}
+           "in_dtype": wl.in_dtype, "state_dtype": "f32", "accept_len": wl.accept,
+           # each rank runs its own sequences (a batch shard) with no collective on the data path
+           "parallelism": f"dp{world}" if world > 1 else "single GPU"}
     if nsets is not None:
         cfg["l2"] = (f"{nsets} independent input sets rotated; each set is read again only after more than "
                      f"2x the 126 MB L2 of other traffic")
@@ -1258,7 +1260,7 @@ def main(argv=None):
             "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; no dataset)",
-            "config": dict(workload_config(wl, r["nsets"]), layers_per_launch=r["layers_per_launch"]),
+            "config": dict(workload_config(wl, r["nsets"], world), layers_per_launch=r["layers_per_launch"]),
             "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": r["peak"], "unit": "GB/s",
                          "frac": r["achieved_gbs"] / r["peak"], "traffic": traffic,
                          "peak_source": f"{r['peak_kind']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",

@@ -80,6 +80,7 @@ def test_bench_gpus_2_launches_its_own_ranks(monkeypatch, capfd):
     line = json.loads(lines[0])
     wl = synth.WORKLOADS[0]
     assert line["n_gpus"] == 2 and line["scaling"] == "weak" and line["steps"] == steps
+    assert line["config"]["parallelism"] == "dp2"
     assert abs(line["ms_per_step"] - 11.0 / steps) < 1e-12  # the maximum over the ranks
     want = wl.batch * wl.ntok * 2 * wl.nlayers * steps / 11.0e-3
     assert abs(line["value"] - want) < 1e-9 * want
