@@ -237,7 +237,8 @@ int ssm_step_pool(const ssm_desc_t *desc, const ssm_pool_t *pool, const void *x,
  * ssm_prefill_workspace_bytes -- device workspace that ssm_prefill would use
  * for this shape on the current device (0: it runs in one pass and needs
  * none): batch * (ntok / L) states for the chunk length L it picks, plus a
- * small map of the chunks' slots (4 bytes per chunk, rounded up to 16).
+ * small map of the chunks' slots (4 bytes per chunk) and each chunk's decay
+ * product per head (4 bytes per chunk and head), each rounded up to 16 bytes.
  * L = 128 for bf16 inputs with dstate 128, headdim a multiple of 64 and
  * ntok a multiple of 128 of at least 256 (the tensor-core chunk passes);
  * other shapes chunk only when one pass would not fill the device, with the

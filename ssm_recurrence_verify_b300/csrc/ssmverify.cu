@@ -1176,6 +1176,7 @@ struct CSArgs {
     const void *x, *B, *dt;  // chunk v = tokens v*L .. v*L + L - 1 of the [batch][T] layouts
     const float *A;
     float *ws;               // [chunks][H][P][N]
+    float *lam;              // [chunks][H]: lambda = the product of the chunk's Abar, for the scan
     uint32_t *dev_status;    // nullable (the tensor-memory kernel's bounded wait)
     int H, P, G, L, ptiles;  // ptiles: tiles of a chunk (P / 64 per head; H P / 128 on the tensor cores)
 };
@@ -1235,10 +1236,12 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
         cp_async16(sb + s * LY::kBPad + q * VW, Bp + ((v * L + s) * a.G + gi) * (long long)N + q * VW);
     }
     // dt and the suffix products w_s = prod_{r > s} Abar_r (a fixed product tree)
+    float abar0 = 1.f;
     if (tid < L) {
         const float d = ld1(dtp + (v * L + tid) * a.H + h);
         sdt[tid] = d;
         sw[tid] = tid + 1 < L ? ssm_decay(ld1(dtp + (v * L + tid + 1) * a.H + h), Ah) : 1.f;
+        if (tid == 0) abar0 = ssm_decay(d, Ah);
     }
     __syncthreads();
     float *cur = sw, *nxt = sw2;
@@ -1249,6 +1252,8 @@ __global__ void __launch_bounds__(128) ssm_chunk_state_kernel(const CSArgs a) {
         cur = nxt;
         nxt = tmp;
     }
+    // the chunk's lambda = Abar_0 w_0, once per chunk and head (the head's first row tile)
+    if (tid == 0 && ptile == 0) a.lam[v * a.H + h] = __fmul_rn(abar0, cur[0]);
     cp_async_wait_all();
     __syncthreads();
 
@@ -1393,12 +1398,14 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
         br[i] = __ldg(reinterpret_cast<const uint4 *>(Bp + (bt * a.G + gi) * 128LL + p0));
     }
     // dt and the suffix products w_s = prod_{r > s} Abar_r (the product tree of ssm_chunk_state_kernel), per head
+    float abar0 = 1.f;
     if (tid < nh * L) {
         const int hh = h0 + (tid >> 7), s = tid & (L - 1);
         const float Ah = __ldg(a.A + hh);
         const float d = ld1(dtp + (v * L + s) * a.H + hh);
         sdt[tid] = d;
         sw[tid] = s + 1 < L ? ssm_decay(ld1(dtp + (v * L + s + 1) * a.H + hh), Ah) : 1.f;
+        if (s == 0) abar0 = ssm_decay(d, Ah);
     }
     if (tid == 0) {
         mbar_init(&bar, 1);
@@ -1427,6 +1434,9 @@ __global__ void __launch_bounds__(kTCThreads, 2) ssm_chunk_state_tc_kernel(const
         cur = nxt;
         nxt = tmp;
     }
+    // the chunk's lambda = Abar_0 w_0 of each head whose first row is in this tile (once per chunk and head)
+    if (tid < nh * L && (tid & (L - 1)) == 0 && (long long)(h0 + (tid >> 7)) * a.P >= R0)
+        a.lam[v * a.H + h0 + (tid >> 7)] = __fmul_rn(abar0, cur[tid]);
     // w o U in fp32, split into two bf16 parts, transposed into the A operands (row p0 + j, of head h0 + hf)
     const int hf = nh == 1 ? 0 : p0 / a.P;
     float wsv[8], dsv[8];
@@ -1803,6 +1813,7 @@ struct ScanArgs {
     int nslots;
     float *ws;              // [batch * nch][H][P][N]
     int32_t *vslot;         // [batch * nch]: chunk c of sequence b -> b * nch + c, or -1 for an invalid slot
+    const float *lamw;      // [batch * nch][H]: lambda_c from the first pass, or nullptr: formed here from dt
     const void *dt;         // [batch][T][H]
     int in_bf16;
     const float *A;
@@ -1845,18 +1856,23 @@ __global__ void __launch_bounds__(kScanThreads, 4) ssm_chunk_scan_kernel(const S
         for (int k = 0; k < kScanAhead; ++k)
             if (k < a.nch) S[k] = __ldcs(w + k * cstride);
     }
-    // lambda_c: one warp per chunk, a fixed product tree over the chunk's tokens
-    for (int c = warp; c < a.nch; c += kScanThreads / 32) {
-        float prod = 1.f;
-        for (int i = lane; i < a.L; i += 32) {
-            const long long t = (long long)b * a.nch * a.L + (long long)c * a.L + i;
-            const float dtv = a.in_bf16 ? ld1(static_cast<const __nv_bfloat16 *>(a.dt) + t * a.H + h)
-                                        : ld1(static_cast<const float *>(a.dt) + t * a.H + h);
-            prod = __fmul_rn(prod, ssm_decay(dtv, Ah));
-        }
+    // lambda_c: from the first pass where it formed them, else one warp per chunk, a fixed product tree
+    // over the chunk's tokens
+    if (a.lamw != nullptr) {
+        for (int c = tid; c < a.nch; c += kScanThreads) lam[c] = __ldg(a.lamw + ((long long)b * a.nch + c) * a.H + h);
+    } else {
+        for (int c = warp; c < a.nch; c += kScanThreads / 32) {
+            float prod = 1.f;
+            for (int i = lane; i < a.L; i += 32) {
+                const long long t = (long long)b * a.nch * a.L + (long long)c * a.L + i;
+                const float dtv = a.in_bf16 ? ld1(static_cast<const __nv_bfloat16 *>(a.dt) + t * a.H + h)
+                                            : ld1(static_cast<const float *>(a.dt) + t * a.H + h);
+                prod = __fmul_rn(prod, ssm_decay(dtv, Ah));
+            }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) prod = __fmul_rn(prod, __shfl_xor_sync(~0u, prod, off));
-        if (lane == 0) lam[c] = prod;
+            for (int off = 16; off > 0; off >>= 1) prod = __fmul_rn(prod, __shfl_xor_sync(~0u, prod, off));
+            if (lane == 0) lam[c] = prod;
+        }
     }
     if (!ok && blockIdx.x == 0 && h == 0 && tid == 0 && a.dev_status != nullptr)
         atomicOr(a.dev_status, SSM_STATUS_BAD_SLOT);
@@ -2166,12 +2182,16 @@ int device_sms() {
 constexpr int kMaxChunks = 4096;
 
 // Workspace of a chunked prefill with chunk length L: the chunk states, then
-// the chunks' slot map (16-byte aligned).
+// the chunks' slot map, then each chunk's lambda per head (each part 16-byte
+// aligned).
 int64_t prefill_ws_states(const ssm_desc_t *d, int L) {
     return (int64_t)d->batch * (d->ntok / L) * d->nheads * d->headdim * d->dstate * 4;
 }
-int64_t prefill_ws_bytes(const ssm_desc_t *d, int L) {
+int64_t prefill_ws_lam(const ssm_desc_t *d, int L) {
     return prefill_ws_states(d, L) + ((int64_t)d->batch * (d->ntok / L) * 4 + 15) / 16 * 16;
+}
+int64_t prefill_ws_bytes(const ssm_desc_t *d, int L) {
+    return prefill_ws_lam(d, L) + ((int64_t)d->batch * (d->ntok / L) * d->nheads * 4 + 15) / 16 * 16;
 }
 
 // Chunk length of a chunked prefill: 128 for the shapes of the tensor-memory
@@ -2330,6 +2350,7 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
         ca.dt = dt;
         ca.A = A;
         ca.ws = static_cast<float *>(ws);
+        ca.lam = reinterpret_cast<float *>(static_cast<char *>(ws) + prefill_ws_lam(d, L));
         ca.dev_status = dev_status;
         ca.H = (int)H;
         ca.P = (int)P;
@@ -2358,6 +2379,7 @@ int prefill(const ssm_desc_t *d, const ssm_pool_t *pool, const void *x, const vo
                          ? reinterpret_cast<int32_t *>(static_cast<char *>(ws) + prefill_ws_states(d, L))
                          : nullptr;
     sa.vslot = vslot;
+    sa.lamw = cs_ok ? reinterpret_cast<const float *>(static_cast<const char *>(ws) + prefill_ws_lam(d, L)) : nullptr;
     sa.dt = dt;
     sa.in_bf16 = d->in_dtype == SSM_BF16;
     sa.A = A;

@@ -362,13 +362,18 @@ def test_layer_stack_validation(lib):
 def test_prefill_chunk_rule_for_tensor_core_shapes(lib):
     """bf16 prompts with N = 128, headdim a multiple of 64 and at least two
     128-token chunks take 128-token chunks whatever the device: workspace =
-    batch * (T / 128) states + the chunks' slot map (16-byte rounded). Other
-    shapes chunk only to fill the device, which this host has none of (0)."""
+    batch * (T / 128) states + the chunks' slot map + each chunk's decay
+    product per head (each 16-byte rounded). Other shapes chunk only to fill
+    the device, which this host has none of (0)."""
     def ws(**kw):
         return lib.ssm_prefill_workspace_bytes(ctypes.byref(desc(**kw)))
 
+    def r16(n):
+        return (n + 15) // 16 * 16
+
     def want(batch, T, H, P):
-        return batch * (T // 128) * H * P * 128 * 4 + (batch * (T // 128) * 4 + 15) // 16 * 16
+        nch = batch * (T // 128)
+        return nch * H * P * 128 * 4 + r16(nch * 4) + r16(nch * H * 4)
 
     for P in (64, 128, 192, 256):
         assert ws(batch=1, nheads=80, headdim=P, ngroups=1, ntok=2048) == want(1, 2048, 80, P), P
