@@ -1830,7 +1830,8 @@ __device__ __forceinline__ float4 fma4(float l, float4 h, float4 s) {
     return make_float4(fmaf(l, h.x, s.x), fmaf(l, h.y, s.y), fmaf(l, h.z, s.z), fmaf(l, h.w, s.w));
 }
 
-__global__ void __launch_bounds__(kScanThreads, 4) ssm_chunk_scan_kernel(const ScanArgs a) {
+// (launch bounds of two CTAs per SM: the register budget of four spilled the eight chunk vectors in flight)
+__global__ void __launch_bounds__(kScanThreads, 2) ssm_chunk_scan_kernel(const ScanArgs a) {
     extern __shared__ float lam[];  // [nch]
     const int b = blockIdx.z, h = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
