@@ -139,6 +139,21 @@ def algorithmic_bytes(wl: synth.Workload, batch: int, accepted_nonzero: int) -> 
             + batch * K * H * P * 4 + (0 if wl.accept == "all" else batch * 4))
 
 
+def algorithmic_bytes_commit_verify(wl: synth.Workload, batch: int, accept_len) -> int:
+    """What one deferred-commit layer-call (ssm_commit_verify) must move: the
+    state read once and written for sequences with j_prev > 0, the previous
+    block's x / B / dt for its j_prev accepted tokens only (B once per group),
+    the new block's x / B / C / dt, y of the new block in fp32, and
+    accept_len_prev."""
+    H, P, N, G, K = wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.ntok
+    eb = wl.in_elem_bytes()
+    slice_b = H * P * N * 4
+    js = [int(j) for j in accept_len]
+    replay = sum(js) * (H * P * eb + G * N * eb + H * eb)
+    return (batch * slice_b + sum(1 for j in js if j > 0) * slice_b + replay
+            + batch * K * (H * P * eb + 2 * G * N * eb + H * eb) + batch * K * H * P * 4 + batch * 4)
+
+
 def tile_tensor_macs(wl: synth.Workload, accept_len, layers: int) -> int:
     """Multiply-adds one fused verify+commit launch issues on the tensor cores
     (mma.sync m16n8k8 tf32, 1024 each), at N <= 128 (one warp per 16-row band):
@@ -398,17 +413,21 @@ class LayerSet:
     y and status as [L]-leading slabs (`stack`; accept_len [batch] is shared
     by the layers), and per layer views of them (`layers`)."""
 
-    def __init__(self, wl, batch, offset, rnd, dev, layers):
+    def __init__(self, wl, batch, offset, rnd, dev, layers, next_round=False):
         ds = [synth.draw_layer_round(wl, rnd=rnd, layer=layer, batch=batch, batch_offset=offset)
               for layer in range(layers)]
         self.stack = {k: torch.stack([d[k] for d in ds]).to(dev) for k in ("state0", "x", "B", "C", "dt", "A", "D")}
+        if next_round:  # the next round's drafts: the new block of a deferred commit (this round's is the previous)
+            nx = [synth.draw_tokens(wl, rnd + 1, layer, batch, offset) for layer in range(layers)]
+            for k in ("x", "B", "C", "dt"):
+                self.stack[k + "2"] = torch.stack([d[k] for d in nx]).to(dev)
         self.stack["accept_len"] = ds[0]["accept_len"].to(dev)  # one accepted prefix per sequence, every layer
         self.stack["y"] = torch.empty((layers, batch, wl.ntok, wl.nheads, wl.headdim), dtype=torch.float32,
                                       device=dev)
         self.stack["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
         self.layers = []
         for layer, d in enumerate(ds):
-            e = {k: self.stack[k][layer] for k in ("state0", "x", "B", "C", "dt", "A", "D", "y")}
+            e = {k: v[layer] for k, v in self.stack.items() if k not in ("accept_len", "status")}
             e["accept_len"] = self.stack["accept_len"]
             e["status"] = self.stack["status"]
             e["host"] = d
@@ -416,10 +435,15 @@ class LayerSet:
             self.layers.append(e)
 
 
-def launch_layer(ssm, wl, e):
+def launch_layer(ssm, wl, e, deferred=False):
     """One layer-call (per-layer tensors), or one call over the whole stack
-    (the [L]-leading slabs of LayerSet.stack)."""
-    if wl.accept == "all" and wl.ntok == 1:
+    (the [L]-leading slabs of LayerSet.stack). deferred: the serving order's
+    ssm_commit_verify, which commits this set's round (its drafts and
+    accept_len) and verifies the next round's drafts from the committed state."""
+    if deferred:
+        ssm.commit_verify(e["state0"], e["x"], e["B"], e["dt"], e["accept_len"], e["x2"], e["B2"], e["C2"], e["dt2"],
+                          e["A"], e["D"], y=e["y"], dev_status=e["status"])
+    elif wl.accept == "all" and wl.ntok == 1:
         ssm.step(e["state0"], e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], y=e["y"])
     else:
         ssm.verify_commit(e["state0"], e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], e["accept_len"], y=e["y"],
@@ -442,7 +466,8 @@ def device_leg(args, wl, rank, world, local_rank):
     nl = wl.nlayers
     step_bytes_est = nl * (2 * batch * wl.nheads * wl.headdim * wl.dstate * 4)
     nsets = 1 if step_bytes_est >= 4 * L2_BYTES else max(3, math.ceil(2 * L2_BYTES / step_bytes_est) + 1)
-    sets = [LayerSet(wl, batch, offset, rnd, dev, nl) for rnd in range(nsets)]
+    deferred = getattr(args, "path", "ssm") == "commit_verify"
+    sets = [LayerSet(wl, batch, offset, rnd, dev, nl, next_round=deferred) for rnd in range(nsets)]
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     # a layer stack runs as one launch per step (nlayers = L), unless asked per layer
@@ -453,7 +478,7 @@ def device_leg(args, wl, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for s in sets:
             for e in units(s):
-                launch_layer(ssm, wl, e)
+                launch_layer(ssm, wl, e, deferred)
     torch.cuda.synchronize()
 
     # The warm-up steps and the K timed steps are captured as CUDA graphs
@@ -467,7 +492,7 @@ def device_leg(args, wl, rank, world, local_rank):
             with torch.cuda.graph(g, stream=stream):
                 for si in step_sets[i:i + per]:
                     for e in units(sets[si]):
-                        launch_layer(ssm, wl, e)
+                        launch_layer(ssm, wl, e, deferred)
             out.append(g)
         return out
 
@@ -502,10 +527,14 @@ def device_leg(args, wl, rank, world, local_rank):
         for e in s.layers:
             assert int(e["status"].item()) == 0, "device reported a bad accept_len"
     # per-step algorithmic bytes, averaged over the sets the timed steps used
-    step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
+    if deferred:
+        step_bytes = [sum(algorithmic_bytes_commit_verify(wl, batch, e["host"]["accept_len"]) for e in s.layers)
+                      for s in sets]
+    else:
+        step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
     used = [step_bytes[si] for si in timed_sets]
-    step_macs = [tile_tensor_macs(wl, s.layers[0]["host"]["accept_len"], nl) for s in sets]
-    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 else None
+    step_macs = [0 if deferred else tile_tensor_macs(wl, s.layers[0]["host"]["accept_len"], nl) for s in sets]
+    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 and not deferred else None
     return {"elapsed_ms": elapsed_ms, "steps": K, "per_step": per_step, "batch": batch, "nsets": nsets,
             "launch_bytes": statistics.fmean(used) / per_step,
             "launch_macs": statistics.fmean(step_macs[si] for si in timed_sets) / per_step,
@@ -1169,6 +1198,29 @@ def tensor_line(r, wl):
             "peak_source": f"{kind} bf16 dense x {TF32_PER_BF16:.3f} (nominal tf32 / bf16 ratio)"}
 
 
+def commit_verify_line(args, wl, r, world):
+    """The JSON line of --path commit_verify: the verify/commit workload in the
+    serving order (ssm_commit_verify), device-timed like the default path,
+    with the HBM roofline on what the deferred-commit call must move."""
+    return {
+        "metric": "draft tokens verified/s per SSM layer, deferred-commit order (ssm_commit_verify); "
+                  "achieved HBM GB/s vs B300 peak",
+        "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; no dataset)", "path": "commit_verify",
+        "config": dict(workload_config(wl, r["nsets"], world), layers_per_launch=r["layers_per_launch"],
+                       previous_block="the set's own round (its drafts and accept_len)",
+                       new_block="the next round's drafts"),
+        "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": r["peak"], "unit": "GB/s",
+                     "frac": r["achieved_gbs"] / r["peak"], "traffic": None,
+                     "peak_source": f"{r['peak_kind']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": r["bytes_per_launch"],
+                     "launch_us_mean": r["launch_ms_mean"] * 1e3,
+                     "frac_of_8tbs_spec": r["achieved_gbs"] / HBM_SPEC_GBS},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": r["launches"], "clocks": r["clocks"],
+    }
+
+
 def workload_config(wl, nsets, world: int = 1):
     cfg = {"workload": wl.name, "batch_per_gpu": wl.batch, "layers": wl.nlayers, "nheads": wl.nheads,
            "headdim": wl.headdim, "dstate": wl.dstate, "ngroups": wl.ngroups, "draft_tokens": wl.ntok,
@@ -1200,8 +1252,11 @@ def main(argv=None):
                     help="run only the first N layers of a layer stack (a smaller case for profiling)")
     ap.add_argument("--per-layer-launches", action="store_true",
                     help="run a layer stack as one launch per layer instead of one launch over all layers")
-    ap.add_argument("--path", choices=["ssm", "accept_sample", "accept_greedy", "prefill", "e2e_pieces"], default="ssm",
-                    help="ssm: the verify/commit step (default); accept_*: the acceptance step alone; "
+    ap.add_argument("--path", choices=["ssm", "commit_verify", "accept_sample", "accept_greedy", "prefill", "e2e_pieces"],
+                    default="ssm",
+                    help="ssm: the verify/commit step (default); commit_verify: the same workload in the serving "
+                         "order, each call committing the previous round's accepted prefix and verifying the next "
+                         "round's drafts (ssm_commit_verify); accept_*: the acceptance step alone; "
                          "prefill: a 2048-token prompt through one layer; e2e_pieces: the host-buffer step of the "
                          "workload taken apart (copies in, read-back, kernels, each alone and together)")
     ap.add_argument("--prefill-dtype", choices=["bf16", "f32"], default="bf16",
@@ -1228,7 +1283,7 @@ def main(argv=None):
 
     if world > 1:
         init_ranks(world, local_rank)
-    if args.path != "ssm":
+    if args.path not in ("ssm", "commit_verify"):
         if args.path == "prefill":
             line = run_prefill(args, rank, world, local_rank)
         elif args.path == "e2e_pieces":
@@ -1242,6 +1297,14 @@ def main(argv=None):
             dist.destroy_process_group()
         return 0
     r = run_ours(args, wl, rank, world, local_rank)
+
+    if args.path == "commit_verify":
+        if rank == 0:
+            print(json.dumps(commit_verify_line(args, wl, r, world)), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
 
     cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

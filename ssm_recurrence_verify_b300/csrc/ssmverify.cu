@@ -130,6 +130,9 @@ struct Lay {
     static constexpr int ROWS = G::kRows;
     static constexpr bool R = Flav<F>::kReplay;
     static constexpr bool V = Flav<F>::kVerifyPhase;
+    // the replay's first chunk travels with the tile's copies only in the commit-only flavour; the
+    // deferred-commit flavours stage it from global memory into the verify phase's arrays (below)
+    static constexpr bool RR = R && !V;
     static constexpr int E = (int)sizeof(Tin);
     static constexpr int BC = kTC * G::kWPB * 4 * G::kPad * 4;        // one permuted B or C chunk
     static constexpr int kState = 0;                                    // float [ROWS][N]
@@ -138,8 +141,8 @@ struct Lay {
     static constexpr int oVB = oVx + (V ? kTC * ROWS * E : 0);          // Tin [kTC][N]
     static constexpr int oVC = oVB + (V ? kTC * N * E : 0);             // Tin [kTC][N]
     static constexpr int oRx = oVC + (V ? kTC * N * E : 0);             // Tin [kTC][ROWS]
-    static constexpr int oRB = oRx + (R ? kTC * ROWS * E : 0);          // Tin [kTC][N]
-    static constexpr int kRawBytes = oRB + (R ? kTC * N * E : 0);
+    static constexpr int oRB = oRx + (RR ? kTC * ROWS * E : 0);         // Tin [kTC][N]
+    static constexpr int kRawBytes = oRB + (RR ? kTC * N * E : 0);
     static constexpr int kRaw = kState + ROWS * N * 4;                  // 2 raw buffers
     static constexpr int kVB = kRaw + 2 * kRawBytes;                    // float, permuted
     static constexpr int kVC = kVB + (V ? BC : 0);                      // float, permuted
@@ -149,10 +152,13 @@ struct Lay {
     static constexpr int kVCs = kVAbar + (V ? kTC * 4 : 0);             // float [kTC]
     static constexpr int kVW = kVCs + (V ? kTC * 4 : 0);                // float [kTC]
     static constexpr int kXch = kVW + (V ? kTC * 4 : 0);                // float [bands][32][8] (N = 256)
-    static constexpr int kRB = kXch + (V && G::kWPB > 1 ? G::kBands * 32 * 8 * 4 : 0);  // float, permuted
-    static constexpr int kRU = kRB + (R ? BC : 0);                      // float [kTC][kUS]
-    static constexpr int kRAbar = kRU + (R ? kTC * G::kUS * 4 : 0);     // float [kTC]
-    static constexpr int kBytes = kRAbar + (R ? kTC * 4 : 0);
+    static constexpr int kXchEnd = kXch + (V && G::kWPB > 1 ? G::kBands * 32 * 8 * 4 : 0);
+    // the replay's staged arrays: their own, or with a verify phase the verify phase's, which is
+    // staged only once the replay is done
+    static constexpr int kRB = V ? kVB : kXchEnd;                       // float, permuted
+    static constexpr int kRU = V ? kVU : kRB + (R ? BC : 0);            // float [kTC][kUS]
+    static constexpr int kRAbar = V ? kVAbar : kRU + (R ? kTC * G::kUS * 4 : 0);  // float [kTC]
+    static constexpr int kBytes = V ? kXchEnd : kRAbar + (R ? kTC * 4 : 0);
     static_assert(kRawBytes % 16 == 0 && kRaw % 128 == 0, "bulk-copy destinations must be 16-byte aligned");
 };
 
@@ -484,16 +490,40 @@ __device__ __forceinline__ ChunkDt load_chunk_dt(const Args &a, const Block &blk
     return d;
 }
 
+// The x and B items of one thread for a replay chunk, loaded from global memory
+// before the tile's state arrives (N <= 128: at most one item of each per thread).
+template <typename Tin>
+struct PreItems {
+    Raw8<Tin> x, b;
+};
+template <typename Tin, int N>
+__device__ __forceinline__ PreItems<Tin> load_items(const Args &a, const Block &blk, const Tile &T, int tc) {
+    constexpr int XPT = Geo<N>::kRows / 8, BPT = N / 8;
+    static_assert(kTC * BPT <= kThreads, "one B item per thread");
+    const int tid = threadIdx.x;
+    const long long bt0 = T.b * blk.K;
+    PreItems<Tin> p;
+    const int t = tid / XPT, r8 = tid % XPT;
+    if (tid < kTC * XPT && t < tc)
+        ld8(static_cast<const Tin *>(blk.x) + ((bt0 + t) * a.H + T.h) * a.P + T.row0 + 8 * r8, blk.vec_x,
+            T.rows - 8 * r8, p.x);
+    const int tb = tid / BPT, n8 = tid % BPT;
+    if (tid < kTC * BPT && tb < tc)
+        ld8(static_cast<const Tin *>(blk.B) + ((bt0 + tb) * a.G + T.g) * N + 8 * n8, blk.vec_bc, 8, p.b);
+    return p;
+}
+
 // Convert one chunk of tc tokens into the staged fp32 arrays, from the raw
 // rows in shared memory (FROM_RAW: offsets rawX / rawB / rawC) or from global
 // memory. x items are 8 rows of one token (u = dt x and D x), B/C items 8
 // columns of one token. Tokens tc .. kTC-1 of u and B are zeroed (they meet
-// zero weights in the contractions over the chunk and must not be NaN). Warp 0 also
-// forms Abar, cs_t = sum_{r<=t} dt_r and w_t = exp(A cs_t) (verify phase).
-template <typename Tin, int N, bool WANT_Y, bool FROM_RAW>
+// zero weights in the contractions over the chunk and must not be NaN). The last
+// warp also forms Abar, cs_t = sum_{r<=t} dt_r and w_t = exp(A cs_t) (verify phase).
+// PRE: the x / B items come from load_items, issued earlier (global memory).
+template <typename Tin, int N, bool WANT_Y, bool FROM_RAW, bool PRE = false>
 __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, const Tile &T, int t0, int tc, float Ah,
                                             float Dh, const StagedOffsets &so, int rawX, int rawB, int rawC,
-                                            const ChunkDt &dt) {
+                                            const ChunkDt &dt, const PreItems<Tin> *pre = nullptr) {
     constexpr int ROWS = Geo<N>::kRows;
     constexpr int XPT = ROWS / 8;  // x items per token
     constexpr int BPT = N / 8;     // B/C items per token
@@ -512,7 +542,8 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
         if (t < tc) {
             Raw8<Tin> r;
             const long long row = (bt0 + t) * a.H + T.h;
-            if (FROM_RAW) lds8(sm<const Tin>(rawX) + t * ROWS + 8 * r8, r);
+            if constexpr (PRE) r = pre->x;
+            else if (FROM_RAW) lds8(sm<const Tin>(rawX) + t * ROWS + 8 * r8, r);
             else ld8(xp + row * a.P + T.row0 + 8 * r8, blk.vec_x, T.rows - 8 * r8, r);
             widen(r, xv);
 #pragma unroll
@@ -549,7 +580,8 @@ __device__ __forceinline__ void stage_chunk(const Args &a, const Block &blk, con
         }
         Raw8<Tin> r;
         float v[8];
-        if (FROM_RAW) lds8(sm<const Tin>(rawB) + t * N + 8 * n8, r);
+        if constexpr (PRE) r = pre->b;
+        else if (FROM_RAW) lds8(sm<const Tin>(rawB) + t * N + 8 * n8, r);
         else ld8(Bp + off, blk.vec_bc, 8, r);
         widen(r, v);
         st_slots<N>(sm<float>(so.B) + p0, v[0], v[1], v[2], v[3]);
@@ -894,14 +926,17 @@ __device__ __forceinline__ long long next_work(const Args &a, long long t) {
 #ifndef SSM_REGCAP
 #define SSM_REGCAP 128
 #endif
-// Register budget per thread (resident CTAs of 128 threads = 65536 / (128 x cap)).
-template <int N, int F>
+// Register budget per thread (resident CTAs of 128 threads = 65536 / (128 x cap)),
+// or that of the CTAs the flavour's shared memory lets reside, if fewer.
+template <typename Tin, int N, int F>
 constexpr int min_blocks() {
-    return 65536 / SSM_REGCAP / kThreads > 0 ? 65536 / SSM_REGCAP / kThreads : 1;
+    constexpr int by_regs = 65536 / SSM_REGCAP / kThreads > 0 ? 65536 / SSM_REGCAP / kThreads : 1;
+    constexpr int by_smem = (228 * 1024) / (Lay<Tin, N, F>::kBytes + 1024);
+    return by_smem < 1 ? 1 : (by_smem < by_regs ? by_smem : by_regs);
 }
 
 template <typename Tin, int N, int F>
-__global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, (min_blocks<Tin, N, F>())) ssm_tile_kernel(const Args a) {
     using G = Geo<N>;
     using FL = Flav<F>;
     using LY = Lay<Tin, N, F>;
@@ -941,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
     auto plan = [&](const Tile &T, long long tt, int buf) {
         Plan pl{nullptr, 0u, 0u, 0u};
         if (tt >= a.ntiles) return pl;
-        const int tcR = FL::kReplay && a.rep.tma ? min(accepted(a, T.bs, a.rep.K), kTC) : 0;
+        const int tcR = LY::RR && a.rep.tma ? min(accepted(a, T.bs, a.rep.K), kTC) : 0;
         const int tcV = FL::kVerifyPhase && a.ver.tma ? min(a.ver.K, kTC) : 0;
         const uint32_t xrow = (uint32_t)T.rows * E, bcrow = (uint32_t)N * E;
         pl.total = (FL::kZero ? 0u : (uint32_t)T.rows * N * 4) + tcR * (xrow + bcrow) + tcV * (xrow + 2 * bcrow);
@@ -1025,6 +1060,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         cur = load_in(Tn, tn);
         Tcur = Tn;
 
+        // Deferred-commit flavours at N <= 128: the replay chunk's x / B items are loaded
+        // before the wait, while no state registers are live, so their latency overlaps it.
+        constexpr bool kPre = FL::kReplay && FL::kVerifyPhase && kTC * (N / 8) <= kThreads;
+        PreItems<Tin> pre;
+        if constexpr (kPre)
+            if (jr > 0) pre = load_items<Tin, N>(a, a.rep, T, tcR0);
         // Wait for the tile's bulk copies; the state tile goes to registers.
         const bool ok = mbar_wait_bounded(&bar, parity);
         float2 hs[2][G::kNC / 2];
@@ -1052,14 +1093,16 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
         const int raw = LY::kRaw + (int)parity * LY::kRawBytes;
         if constexpr (FL::kReplay) {
             if (jr > 0) {
-                if (a.rep.tma)
+                if (LY::RR && a.rep.tma)
                     stage_chunk<Tin, N, false, true>(a, a.rep, T, 0, tcR0, Ah, 0.f, sR, raw + LY::oRx, raw + LY::oRB,
                                                      raw + LY::oRB, dR);
+                else if constexpr (kPre)
+                    stage_chunk<Tin, N, false, false, true>(a, a.rep, T, 0, tcR0, Ah, 0.f, sR, 0, 0, 0, dR, &pre);
                 else
                     stage_chunk<Tin, N, false, false>(a, a.rep, T, 0, tcR0, Ah, 0.f, sR, 0, 0, 0, dR);
             }
         }
-        if constexpr (FL::kVerifyPhase) {
+        if constexpr (FL::kVerifyPhase && !FL::kReplay) {
             if (a.ver.tma)
                 stage_chunk<Tin, N, true, true>(a, a.ver, T, 0, tcV0, Ah, Dh, sV, raw + LY::oVx, raw + LY::oVB,
                                                 raw + LY::oVC, dV);
@@ -1096,6 +1139,16 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<N, F>())) ssm_tile_kerne
                 }
             }
             if (jr > 0) store_state<N>(hs, L, sl, T.rows);
+        }
+        if constexpr (FL::kReplay && FL::kVerifyPhase) {
+            // the verify phase's first chunk, into the arrays the replay has finished reading
+            __syncthreads();
+            if (a.ver.tma)
+                stage_chunk<Tin, N, true, true>(a, a.ver, T, 0, tcV0, Ah, Dh, sV, raw + LY::oVx, raw + LY::oVB,
+                                                raw + LY::oVC, dV);
+            else
+                stage_chunk<Tin, N, true, false>(a, a.ver, T, 0, tcV0, Ah, Dh, sV, 0, 0, 0, dV);
+            __syncthreads();
         }
 
         if constexpr (FL::kVerifyPhase) {

@@ -198,6 +198,24 @@ def test_prefill_tensor_work_by_hand():
     assert bench.prefill_tensor_macs(1, 64, 256, 256, 128, False)[0] is None
 
 
+def test_commit_verify_bytes_by_hand():
+    """The deferred-commit call's algorithmic bytes on the serving shapes
+    (H 32, P = N 128, G 8, K 8, bf16), two sequences with j_prev = 0 and 3:
+    both states read (2 x 2 MiB), one written (j_prev > 0), the 3 accepted
+    previous tokens' x (8192 B), B (one group row, 2048 B) and dt (64 B),
+    both sequences' new x / B / C / dt, y in fp32 and accept_len."""
+    wl = synth.WORKLOADS[3]
+    state = 2 * (32 * 128 * 128 * 4)
+    write = 1 * (32 * 128 * 128 * 4)
+    replay = 3 * (8192 + 2048 + 64)
+    new = 2 * 8 * (8192 + 2 * 2048 + 64)
+    y = 2 * 8 * 32 * 128 * 4
+    assert bench.algorithmic_bytes_commit_verify(wl, 2, [0, 3]) == state + write + replay + new + y + 2 * 4 == 6782152
+    # with every previous token accepted the replay reads the whole previous block
+    full = bench.algorithmic_bytes_commit_verify(wl, 2, [8, 8])
+    assert full == state + state + 16 * (8192 + 2048 + 64) + new + y + 8  # both read, both written
+
+
 def test_tile_tensor_work_by_hand():
     """mma.sync work of one launch, K 16 (two 8-token chunks), N 128, bf16, one
     16-row band: y per chunk 16 x 2 + 16 x 1 + 3 = 51 mma, a state update 16 x 2
