@@ -52,6 +52,8 @@ from ssm_recurrence_verify_b300 import synth  # noqa: E402
 
 L2_BYTES = 126 * 1000 * 1000
 MAX_GRAPH_LAUNCHES = 4096  # kernel launches captured per CUDA graph in the timed region
+# --path values that time the verify/commit workload, and the entry points each launches (launch_layer)
+PATH_MODES = {"ssm": "fused", "commit_verify": "deferred", "unfused": "unfused"}
 E2E_STEPS_PER_GRAPH = 16   # consecutive host-buffer steps per CUDA graph in the end-to-end measurement
 HBM_SPEC_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
@@ -152,6 +154,21 @@ def algorithmic_bytes_commit_verify(wl: synth.Workload, batch: int, accept_len) 
     replay = sum(js) * (H * P * eb + G * N * eb + H * eb)
     return (batch * slice_b + sum(1 for j in js if j > 0) * slice_b + replay
             + batch * K * (H * P * eb + 2 * G * N * eb + H * eb) + batch * K * H * P * 4 + batch * 4)
+
+
+def algorithmic_bytes_unfused(wl: synth.Workload, batch: int, accept_len) -> int:
+    """What the unfused pair ssm_verify + ssm_commit must move for one
+    layer-call: verify reads every state, x / B / C / dt and writes y; commit
+    reads the state of each sequence with j > 0 again, its j accepted tokens'
+    x / B / dt and accept_len, and writes that state back."""
+    H, P, N, G, K = wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.ntok
+    eb = wl.in_elem_bytes()
+    slice_b = H * P * N * 4
+    js = [int(j) for j in accept_len]
+    nnz = sum(1 for j in js if j > 0)
+    verify = batch * slice_b + batch * K * (H * P * eb + 2 * G * N * eb + H * eb) + batch * K * H * P * 4
+    commit = 2 * nnz * slice_b + sum(js) * (H * P * eb + G * N * eb + H * eb) + batch * 4
+    return verify + commit
 
 
 def tile_tensor_macs(wl: synth.Workload, accept_len, layers: int) -> int:
@@ -435,12 +452,17 @@ class LayerSet:
             self.layers.append(e)
 
 
-def launch_layer(ssm, wl, e, deferred=False):
+def launch_layer(ssm, wl, e, mode="fused"):
     """One layer-call (per-layer tensors), or one call over the whole stack
-    (the [L]-leading slabs of LayerSet.stack). deferred: the serving order's
+    (the [L]-leading slabs of LayerSet.stack). mode "fused": ssm_verify_commit
+    (ssm_step for plain decode); "deferred": the serving order's
     ssm_commit_verify, which commits this set's round (its drafts and
-    accept_len) and verifies the next round's drafts from the committed state."""
-    if deferred:
+    accept_len) and verifies the next round's drafts from the committed state;
+    "unfused": ssm_verify then ssm_commit, two launches."""
+    if mode == "unfused":
+        ssm.verify(e["state0"], e["x"], e["B"], e["C"], e["dt"], e["A"], e["D"], y=e["y"], dev_status=e["status"])
+        ssm.commit(e["state0"], e["x"], e["B"], e["dt"], e["A"], e["accept_len"], dev_status=e["status"])
+    elif mode == "deferred":
         ssm.commit_verify(e["state0"], e["x"], e["B"], e["dt"], e["accept_len"], e["x2"], e["B2"], e["C2"], e["dt2"],
                           e["A"], e["D"], y=e["y"], dev_status=e["status"])
     elif wl.accept == "all" and wl.ntok == 1:
@@ -466,8 +488,8 @@ def device_leg(args, wl, rank, world, local_rank):
     nl = wl.nlayers
     step_bytes_est = nl * (2 * batch * wl.nheads * wl.headdim * wl.dstate * 4)
     nsets = 1 if step_bytes_est >= 4 * L2_BYTES else max(3, math.ceil(2 * L2_BYTES / step_bytes_est) + 1)
-    deferred = getattr(args, "path", "ssm") == "commit_verify"
-    sets = [LayerSet(wl, batch, offset, rnd, dev, nl, next_round=deferred) for rnd in range(nsets)]
+    mode = PATH_MODES.get(getattr(args, "path", "ssm"), "fused")
+    sets = [LayerSet(wl, batch, offset, rnd, dev, nl, next_round=mode == "deferred") for rnd in range(nsets)]
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     # a layer stack runs as one launch per step (nlayers = L), unless asked per layer
@@ -478,21 +500,21 @@ def device_leg(args, wl, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for s in sets:
             for e in units(s):
-                launch_layer(ssm, wl, e, deferred)
+                launch_layer(ssm, wl, e, mode)
     torch.cuda.synchronize()
 
     # The warm-up steps and the K timed steps are captured as CUDA graphs
     # (step i uses input set i mod nsets; at most MAX_GRAPH_LAUNCHES launches
     # per graph) and replayed back to back, as a serving loop runs its layers.
     def capture(step_sets):
-        per = max(1, MAX_GRAPH_LAUNCHES // per_step)
+        per = max(1, MAX_GRAPH_LAUNCHES // (per_step * (2 if mode == "unfused" else 1)))
         out = []
         for i in range(0, len(step_sets), per):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for si in step_sets[i:i + per]:
                     for e in units(sets[si]):
-                        launch_layer(ssm, wl, e, deferred)
+                        launch_layer(ssm, wl, e, mode)
             out.append(g)
         return out
 
@@ -527,18 +549,21 @@ def device_leg(args, wl, rank, world, local_rank):
         for e in s.layers:
             assert int(e["status"].item()) == 0, "device reported a bad accept_len"
     # per-step algorithmic bytes, averaged over the sets the timed steps used
-    if deferred:
+    if mode == "deferred":
         step_bytes = [sum(algorithmic_bytes_commit_verify(wl, batch, e["host"]["accept_len"]) for e in s.layers)
+                      for s in sets]
+    elif mode == "unfused":
+        step_bytes = [sum(algorithmic_bytes_unfused(wl, batch, e["host"]["accept_len"]) for e in s.layers)
                       for s in sets]
     else:
         step_bytes = [sum(algorithmic_bytes(wl, batch, e["accepted_nonzero"]) for e in s.layers) for s in sets]
     used = [step_bytes[si] for si in timed_sets]
-    step_macs = [0 if deferred else tile_tensor_macs(wl, s.layers[0]["host"]["accept_len"], nl) for s in sets]
-    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 and not deferred else None
+    step_macs = [tile_tensor_macs(wl, s.layers[0]["host"]["accept_len"], nl) if mode == "fused" else 0 for s in sets]
+    e2e = run_e2e(ssm, args, wl, sets[0], stream, dev, world) if args.e2e_steps > 0 and mode == "fused" else None
     return {"elapsed_ms": elapsed_ms, "steps": K, "per_step": per_step, "batch": batch, "nsets": nsets,
             "launch_bytes": statistics.fmean(used) / per_step,
             "launch_macs": statistics.fmean(step_macs[si] for si in timed_sets) / per_step,
-            "wall_s": wall1 - wall0, "graphs": len(timed_graphs),
+            "wall_s": wall1 - wall0, "graphs": len(timed_graphs), "kernels_per_call": 2 if mode == "unfused" else 1,
             "clocks": sampler.summary(wall0, wall1), "e2e": e2e}
 
 
@@ -560,7 +585,8 @@ def run_ours(args, wl, rank, world, local_rank):
         "launch_ms_mean": mean_launch_ms, "graphs": leg["graphs"],
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "bytes_per_launch": leg["launch_bytes"],
         "macs_per_launch": leg.get("launch_macs", 0),
-        "clocks": leg["clocks"], "nsets": leg["nsets"], "e2e": leg["e2e"], "launches": K * per_step,
+        "clocks": leg["clocks"], "nsets": leg["nsets"], "e2e": leg["e2e"],
+        "launches": K * per_step * leg.get("kernels_per_call", 1),
         "batch": leg["batch"], "layers_per_launch": nl // per_step,
     }
 
@@ -1198,19 +1224,29 @@ def tensor_line(r, wl):
             "peak_source": f"{kind} bf16 dense x {TF32_PER_BF16:.3f} (nominal tf32 / bf16 ratio)"}
 
 
-def commit_verify_line(args, wl, r, world):
-    """The JSON line of --path commit_verify: the verify/commit workload in the
-    serving order (ssm_commit_verify), device-timed like the default path,
-    with the HBM roofline on what the deferred-commit call must move."""
+ALT_PATHS = {
+    "commit_verify": ("draft tokens verified/s per SSM layer, deferred-commit order (ssm_commit_verify); "
+                      "achieved HBM GB/s vs B300 peak",
+                      {"previous_block": "the set's own round (its drafts and accept_len)",
+                       "new_block": "the next round's drafts"}),
+    "unfused": ("draft tokens verified/s per SSM layer, unfused (ssm_verify then ssm_commit, two launches per "
+                "layer-call); achieved HBM GB/s vs B300 peak over the pair",
+                {"launches_per_layer_call": 2}),
+}
+
+
+def alt_path_line(args, wl, r, world):
+    """The JSON line of --path commit_verify / unfused: the verify/commit
+    workload through another entry point, device-timed like the default path,
+    with the HBM roofline on what those calls must move (for the unfused
+    pair: both launches together, per layer-call)."""
+    metric, extra = ALT_PATHS[args.path]
     return {
-        "metric": "draft tokens verified/s per SSM layer, deferred-commit order (ssm_commit_verify); "
-                  "achieved HBM GB/s vs B300 peak",
+        "metric": metric,
         "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded; no dataset)", "path": "commit_verify",
-        "config": dict(workload_config(wl, r["nsets"], world), layers_per_launch=r["layers_per_launch"],
-                       previous_block="the set's own round (its drafts and accept_len)",
-                       new_block="the next round's drafts"),
+        "dtype": "f32", "data": "synthetic (seeded; no dataset)", "path": args.path,
+        "config": dict(workload_config(wl, r["nsets"], world), layers_per_launch=r["layers_per_launch"], **extra),
         "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": r["peak"], "unit": "GB/s",
                      "frac": r["achieved_gbs"] / r["peak"], "traffic": None,
                      "peak_source": f"{r['peak_kind']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
@@ -1218,7 +1254,8 @@ def commit_verify_line(args, wl, r, world):
                      "launch_us_mean": r["launch_ms_mean"] * 1e3,
                      "frac_of_8tbs_spec": r["achieved_gbs"] / HBM_SPEC_GBS},
         "cpu_baseline": None, "e2e": None, "gpu_launches": r["launches"], "clocks": r["clocks"],
-    }
+    } | ({"note": "roofline.achieved and launch_us_mean are per layer-call: the two launches together"}
+         if args.path == "unfused" else {})
 
 
 def workload_config(wl, nsets, world: int = 1):
@@ -1252,11 +1289,13 @@ def main(argv=None):
                     help="run only the first N layers of a layer stack (a smaller case for profiling)")
     ap.add_argument("--per-layer-launches", action="store_true",
                     help="run a layer stack as one launch per layer instead of one launch over all layers")
-    ap.add_argument("--path", choices=["ssm", "commit_verify", "accept_sample", "accept_greedy", "prefill", "e2e_pieces"],
+    ap.add_argument("--path", choices=["ssm", "commit_verify", "unfused", "accept_sample", "accept_greedy", "prefill",
+                                       "e2e_pieces"],
                     default="ssm",
                     help="ssm: the verify/commit step (default); commit_verify: the same workload in the serving "
                          "order, each call committing the previous round's accepted prefix and verifying the next "
-                         "round's drafts (ssm_commit_verify); accept_*: the acceptance step alone; "
+                         "round's drafts (ssm_commit_verify); unfused: the same workload as ssm_verify then "
+                         "ssm_commit (two launches per layer-call); accept_*: the acceptance step alone; "
                          "prefill: a 2048-token prompt through one layer; e2e_pieces: the host-buffer step of the "
                          "workload taken apart (copies in, read-back, kernels, each alone and together)")
     ap.add_argument("--prefill-dtype", choices=["bf16", "f32"], default="bf16",
@@ -1283,7 +1322,7 @@ def main(argv=None):
 
     if world > 1:
         init_ranks(world, local_rank)
-    if args.path not in ("ssm", "commit_verify"):
+    if args.path not in PATH_MODES:
         if args.path == "prefill":
             line = run_prefill(args, rank, world, local_rank)
         elif args.path == "e2e_pieces":
@@ -1298,9 +1337,9 @@ def main(argv=None):
         return 0
     r = run_ours(args, wl, rank, world, local_rank)
 
-    if args.path == "commit_verify":
+    if args.path != "ssm":
         if rank == 0:
-            print(json.dumps(commit_verify_line(args, wl, r, world)), flush=True)
+            print(json.dumps(alt_path_line(args, wl, r, world)), flush=True)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

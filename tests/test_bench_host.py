@@ -216,6 +216,21 @@ def test_commit_verify_bytes_by_hand():
     assert full == state + state + 16 * (8192 + 2048 + 64) + new + y + 8  # both read, both written
 
 
+def test_unfused_bytes_by_hand():
+    """The unfused pair on the serving shapes, two sequences with j = 0 and 3:
+    verify reads both states and both sequences' x / B / C / dt and writes y;
+    commit reads and writes the one state with j > 0 and reads the 3 accepted
+    tokens' x / B / dt and accept_len."""
+    wl = synth.WORKLOADS[3]
+    slice_b = 32 * 128 * 128 * 4
+    verify = 2 * slice_b + 2 * 8 * (8192 + 2 * 2048 + 64) + 2 * 8 * 32 * 128 * 4
+    commit = 2 * slice_b + 3 * (8192 + 2048 + 64) + 2 * 4
+    assert bench.algorithmic_bytes_unfused(wl, 2, [0, 3]) == verify + commit == 8879304
+    # against the fused call on the same inputs: one more state read and the accepted tokens' inputs again
+    fused = bench.algorithmic_bytes(wl, 2, 1)
+    assert verify + commit - fused == slice_b + 3 * (8192 + 2048 + 64)
+
+
 def test_tile_tensor_work_by_hand():
     """mma.sync work of one launch, K 16 (two 8-token chunks), N 128, bf16, one
     16-row band: y per chunk 16 x 2 + 16 x 1 + 3 = 51 mma, a state update 16 x 2
