@@ -231,6 +231,14 @@ def test_unfused_bytes_by_hand():
     assert verify + commit - fused == slice_b + 3 * (8192 + 2048 + 64)
 
 
+def test_l2_note_says_when_a_workload_is_smaller_than_the_cache():
+    wl = synth.WORKLOADS[3]
+    big = bench.workload_config(wl, 3, 1, reread_bytes=2 * 268 * 10**6)
+    assert "more than 2x the 126 MB L2" in big["l2"]
+    small = bench.workload_config(synth.WORKLOADS[0], bench.NSETS_CAP, 1, reread_bytes=(bench.NSETS_CAP - 1) * 4096)
+    assert "smaller than the cache" in small["l2"] and f"{bench.NSETS_CAP} independent" in small["l2"]
+
+
 def test_tile_tensor_work_by_hand():
     """mma.sync work of one launch, K 16 (two 8-token chunks), N 128, bf16, one
     16-row band: y per chunk 16 x 2 + 16 x 1 + 3 = 51 mma, a state update 16 x 2
