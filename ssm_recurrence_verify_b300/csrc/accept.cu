@@ -350,26 +350,29 @@ struct Weigher {
     }
 };
 
+constexpr int kCkpt = 4;  // checkpoints of a thread's running sum over its run (the draw)
+
 // Walk the run [e_lo, e_hi) of a row in index order, accumulating the weights
-// in one sequential fp32 chain. With FIND, also return the first entry whose
-// position base + chain (rounded as fl(P + fl(T + chain))) exceeds thr with a
-// positive weight, and the last entry with a positive weight.
+// in one sequential fp32 chain that starts at part0, and return the chain's
+// value. `last` gets the last entry with a positive weight. With FIND, `first`
+// gets the first entry whose position base + chain (rounded as
+// fl(P + fl(T + chain))) exceeds thr with a positive weight, and the walk
+// stops there. ck (not FIND): the chain's value before load unit i of the run
+// is stored at ck[(i / seg) kAT] for i a multiple of seg (shared memory).
 template <typename T, bool VEC, bool FIND>
 __device__ float run_weights(const T *prow, const T *qrow, int e_lo, int e_hi, const Weigher &wf, float P, float Tk,
-                             float thr, int &first, int &last) {
-    float part = 0.f;
+                             float thr, int &first, int &last, float part0 = 0.f, float *ck = nullptr, int seg = 1) {
+    float part = part0;
     auto visit = [&](float w, int e) {
         part = __fadd_rn(part, w);
-        if (FIND) {
-            if (w > 0.f) {
-                last = e;
-                if (first < 0 && __fadd_rn(P, __fadd_rn(Tk, part)) > thr) first = e;
-            }
+        if (w > 0.f) {
+            last = e;
+            if (FIND && first < 0 && __fadd_rn(P, __fadd_rn(Tk, part)) > thr) first = e;
         }
     };
     if (VEC) {
-        // groups of two vectors per row, the next group's loads issued before
-        // the current group is consumed
+        // FIND: groups of two vectors per row, the next group's loads issued
+        // before the current group is consumed
         constexpr int W = Logit<T>::W, G = 2;
         const uint4 *pv = reinterpret_cast<const uint4 *>(prow);
         const uint4 *qv = reinterpret_cast<const uint4 *>(qrow);
@@ -383,8 +386,36 @@ __device__ float run_weights(const T *prow, const T *qrow, int e_lo, int e_hi, c
                 rq[k] = ok && wf.resid ? __ldg(qv + v + k) : make_uint4(0, 0, 0, 0);
             }
         };
+        if constexpr (!FIND) {
+            // the sum pass: four vectors of each row per round, all in flight together (the
+            // same registers as two rounds ahead of two)
+            constexpr int G4 = 4;
+            for (int v = vlo; v < vhi; v += G4) {
+                uint4 rp[G4], rq[G4];
+#pragma unroll
+                for (int k = 0; k < G4; ++k) {
+                    const bool ok = v + k < vhi;
+                    rp[k] = ok ? __ldg(pv + v + k) : make_uint4(0, 0, 0, 0);
+                    rq[k] = ok && wf.resid ? __ldg(qv + v + k) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int k = 0; k < G4; ++k) {
+                    if (v + k >= vhi) break;
+                    if (ck != nullptr && (v + k - vlo) % seg == 0) ck[(v + k - vlo) / seg * kAT] = part;
+#pragma unroll
+                    for (int q = 0; q < W / 2; ++q) {
+                        const float2 w = wf.pair(Logit<T>::pair(rp[k], q), Logit<T>::pair(rq[k], q));
+                        const int e = (v + k) * W + 2 * q;
+                        visit(w.x, e);
+                        visit(w.y, e + 1);
+                    }
+                }
+            }
+            return part;
+        }
         if (vlo < vhi) fetch(cp, cq, vlo);
         for (int v = vlo; v < vhi; v += G) {
+            if (FIND && first >= 0) break;
             if (v + G < vhi) fetch(np_, nq, v + G);
 #pragma unroll
             for (int k = 0; k < G; ++k) {
@@ -404,8 +435,11 @@ __device__ float run_weights(const T *prow, const T *qrow, int e_lo, int e_hi, c
             }
         }
     } else {
-        for (int e = e_lo; e < e_hi; ++e)
+        for (int e = e_lo; e < e_hi; ++e) {
+            if (FIND && first >= 0) break;
+            if (!FIND && ck != nullptr && (e - e_lo) % seg == 0) ck[(e - e_lo) / seg * kAT] = part;
             visit(wf(Logit<T>::one(prow + e), wf.resid ? Logit<T>::one(qrow + e) : 0.f), e);
+        }
     }
     return part;
 }
@@ -419,6 +453,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
     __shared__ float cW;                  // this CTA's total weight (read by the whole cluster)
     __shared__ int s_rej, s_bad, s_owner, s_first, s_last;
     __shared__ float s_P, s_thr;
+    __shared__ float ckpt[kCkpt * kAT];  // the draw: each thread's running sum at checkpoints of its run
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -567,8 +602,12 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
     const int n = hi - lo;
     const int per = ((n + kAT - 1) / kAT + W - 1) / W * W;  // a thread's contiguous run
     const int e_lo = min(lo + tid * per, hi), e_hi = min(e_lo + per, hi);
-    int dummy0 = -1, dummy1 = -1;
-    const float s_k = run_weights<T, VEC, false>(prow, qrow, e_lo, e_hi, wf, 0.f, 0.f, 0.f, dummy0, dummy1);
+    int dummy0 = -1, lastpos = -1;
+    // the run in load units (vectors, or elements), cut into at most kCkpt segments
+    const int units = VEC ? (e_hi - e_lo) / W : e_hi - e_lo;
+    const int seg = units > 0 ? (units + kCkpt - 1) / kCkpt : 1;
+    const float s_k = run_weights<T, VEC, false>(prow, qrow, e_lo, e_hi, wf, 0.f, 0.f, 0.f, dummy0, lastpos, 0.f,
+                                                 ckpt + tid, seg);
     // exclusive prefix of the runs over the CTA
     float incl = s_k;
 #pragma unroll
@@ -625,9 +664,20 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kAT, 4) ssm_accept
         __syncthreads();
         const int who = s_first != kNoIndex ? s_first : s_last;
         if (tid == who) {
+            // The test is monotone in the running sum, so no entry before the first segment whose end
+            // passes it can pass: the walk starts there, from the chain's exact value at that point.
+            const int nseg = (units + seg - 1) / seg;
+            int sg = 0;
+            while (sg < nseg) {
+                const float end = sg + 1 < nseg ? ckpt[(sg + 1) * kAT + tid] : s_k;
+                if (__fadd_rn(P, __fadd_rn(Tk, end)) > thr) break;
+                ++sg;
+            }
             int first = -1, last = -1;
-            run_weights<T, VEC, true>(prow, qrow, e_lo, e_hi, wf, P, Tk, thr, first, last);
-            a.next_token[b] = first >= 0 ? first : last;
+            if (sg < nseg)
+                run_weights<T, VEC, true>(prow, qrow, e_lo + sg * seg * (VEC ? W : 1), e_hi, wf, P, Tk, thr, first,
+                                          last, ckpt[sg * kAT + tid]);
+            a.next_token[b] = first >= 0 ? first : lastpos;
         }
     }
     cluster_wait();  // no CTA leaves while another may still read its total
