@@ -147,6 +147,33 @@ def test_sample_equal_models_accept_everything(cuda_device):
     assert (s["accept_len"] == 6).all()
 
 
+@pytest.mark.parametrize("seed", [61, 62, 63])
+def test_sample_sparse_residual_draw(cuda_device, seed):
+    """The draw's rescan when the residual weight sits on a few isolated
+    entries: the draft row equals the verifier row except 10 lower at the
+    verifier's 8 most likely entries, which hold most of p. With each draft
+    token at its row's least likely entry and u = 0.999 every draft is
+    rejected, max(0, p - q) is positive only at those 8
+    entries, scattered over the vocabulary, and the draw lands among them by
+    u_K: the rescanning thread's run is mostly zero-weight segments around
+    one crossing. The oracle pins the token exactly where no rounding near-tie
+    leaves a choice."""
+    d = synth.draw_accept_inputs(synth.custom_accept_workload(24, 2, 32000, BF16, seed=seed))
+    tl = d["target_logits"]
+    ql = tl[:, :2].clone().float()
+    top = torch.topk(tl[:, :2].float(), 8, dim=-1).indices
+    ql.scatter_(-1, top, ql.gather(-1, top) - 10.0)
+    d["draft_logits"] = ql.to(tl.dtype).contiguous()
+    # each draft token at its row's least likely entry: p/q there is 1 minus most of the top-8 mass
+    d["draft_tokens"] = torch.argmin(tl[:, :2].float(), dim=-1).to(d["draft_tokens"].dtype).contiguous()
+    u = torch.rand(d["uniform"].shape, generator=torch.Generator().manual_seed(seed))
+    u[:, :2] = 0.999
+    d["uniform"] = u.to(d["uniform"].dtype).contiguous()
+    want, unique = check_sample(d, cuda_device)
+    assert (want["accept_len"] == 0).all()
+    assert unique.sum() >= 20
+
+
 def test_deterministic_and_stream_ordered(cuda_device):
     d = synth.draw_accept_inputs(synth.custom_accept_workload(12, 8, 40000, BF16, seed=61))
     dev = cuda_device
