@@ -12,7 +12,9 @@ from ssm_recurrence_verify_b300.hostpipe import HostPipeline
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("chunks,slots", [(1, 1), (3, 2), (5, 3)])
+# fewer slots than chunks, as many, the default (twice the chunks), and more slots than that: chunks take
+# the slots in turn across calls, wrapping around over the rounds
+@pytest.mark.parametrize("chunks,slots", [(1, 1), (3, 2), (5, 3), (2, None), (3, 7)])
 def test_pipeline_equals_device_calls(cuda_device, chunks, slots):
     wl = synth.custom_workload(11, 8, 64, 128, 2, 6, synth.BF16, seed=91)
     p = synth.draw_params(wl)
@@ -32,6 +34,7 @@ def test_pipeline_equals_device_calls(cuda_device, chunks, slots):
         assert torch.equal(y, y_ref.cpu()), rnd
         assert torch.equal(st, st_ref), rnd
     assert int(pipe.status.item()) == 0
+    assert pipe.nslots == (2 * pipe.chunks if slots is None else slots)
 
 
 def test_captured_step_equals_device_calls(cuda_device):
