@@ -119,8 +119,9 @@ struct Geo {
 // Dynamic shared memory layout of one flavour (byte offsets, every region a
 // multiple of 16 bytes). The state tile first (bulk copy destination). Two
 // raw buffers, used by alternate tiles: the first chunk's x / B / C rows of
-// each phase as stored in global memory (bulk-copy destinations), so that the
-// next tile's copies can be issued before this tile's rows are converted.
+// the verify phase (of the replay phase in the commit-only flavour) as stored
+// in global memory (bulk-copy destinations), so that the next tile's copies
+// can be issued before this tile's rows are converted.
 // Staged areas (fp32, what the arithmetic reads): B and C with each thread's
 // slots contiguous ([token][warp column half][tq][kPad]), u = dt x and D x
 // per row, Abar, cs (cumulative dt) and w per token.
@@ -965,9 +966,10 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<Tin, N, F>())) ssm_tile_
     if (t >= a.ntiles) return;  // uniform over the CTA
 
     // A tile streams into shared memory as one transaction on `bar`: the state
-    // rows and, where the layout allows, the raw x / B / C rows of each
-    // phase's first chunk. The copies [state, replay x rows, replay B rows,
-    // verify x rows, verify B rows, verify C rows] are spread over the warps
+    // rows and, where the layout allows, the raw x / B / C rows of the first
+    // chunk of the verify phase, or of the replay phase in the commit-only
+    // flavour. The copies [state, replay x rows, replay B rows, verify x rows,
+    // verify B rows, verify C rows] are spread over the warps
     // (copy k to lane k / 4 of warp k % 4); plan() works out this lane's copy
     // (while the state registers are free), issue() fires it, and lane 0 of
     // warp 0 announces the transaction's total bytes (a completion may arrive
@@ -1094,7 +1096,9 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<Tin, N, F>())) ssm_tile_
             issue(next);
         }
         // Stage the first chunk of each phase: from this tile's raw buffer, or
-        // from global memory where the layout does not allow bulk copies.
+        // from global memory where the layout does not allow bulk copies (and,
+        // in the deferred-commit flavours, the replay chunk from the items loaded
+        // before the wait; their verify chunk is staged after the replay).
         const int raw = LY::kRaw + (int)parity * LY::kRawBytes;
         if constexpr (FL::kReplay) {
             if (jr > 0) {
