@@ -45,7 +45,11 @@
  * segments are not all 16-byte aligned) on `stream` (a cudaStream_t passed
  * as void*, NULL = the legacy default stream) on the current device. Calls
  * are asynchronous. ssm_copy_from_host and ssm_copy_from_host_n alone take
- * host pointers (their sources).
+ * host pointers (their sources). Launches of the verify / commit kernel with
+ * no more blocks than the device has SMs (a decode step of a few sequences)
+ * use programmatic dependent launch: the kernel may become resident while the
+ * previous kernel of the stream finishes, and waits for that kernel's
+ * completion before touching memory, so stream order is kept.
  *
  * Errors: the return value is SSM_OK or an SSM_ERR_* code. Argument errors
  * are detected on the host before anything is launched (no device work is
