@@ -388,6 +388,22 @@ def test_prefill_chunk_rule_for_tensor_core_shapes(lib):
         assert ws(**base) == 0, kw
 
 
+
+@no_gpu_only
+def test_tile_count_limit(lib):
+    """A call whose tiles (layers x batch x heads x row tiles) reach 2^31 is a
+    shape error found on the host (the kernels decode tile indices in 32
+    bits); one tile fewer passes validation and fails only at the launch.
+    The fake buffers are spaced 2^47 bytes apart: the state alone is 2^46."""
+    P = ptrs(12, gap=1 << 47)
+    # 64-row tiles at dstate 128: headdim 64 is one row tile per (sequence, head)
+    at = desc(batch=1 << 20, nheads=1 << 11, headdim=64, ngroups=1)
+    assert vc(lib, at, P[:10] + [None]) == sv.SSM_ERR_SHAPE
+    stacked = desc(batch=1 << 10, nheads=1 << 11, headdim=64, ngroups=1, nlayers=1 << 10)
+    assert vc(lib, stacked, P[:10] + [None]) == sv.SSM_ERR_SHAPE
+    below = desc(batch=(1 << 20) - 1, nheads=1 << 11, headdim=64, ngroups=1)
+    assert vc(lib, below, P[:10] + [None]) == sv.SSM_ERR_CUDA
+
 def pool(states, slot=None, nslots=4, reserved=0):
     return sv.PoolDesc(states, slot, nslots, reserved)
 
