@@ -12,9 +12,11 @@ for step-sized transfers on B300 machines.
 Every sequence's state, inputs and outputs are contiguous slices of the batch
 dimension, so chunks need no gathering. A whole step (one or several layers)
 can be captured once into a CUDA graph, so that issuing it costs one graph
-launch instead of dozens of copy, event and kernel calls. The kernels are the
-library's (``ssm_verify_commit`` through the C ABI); this module only orders
-copies and launches.
+launch instead of dozens of copy, event and kernel calls. ``run_deferred``
+runs the serving order instead (``ssm_commit_verify``: commit the previous
+block, whose inputs stay in the device staging slots, then verify the new
+one). The kernels are the library's (through the C ABI); this module only
+orders copies and launches.
 """
 from __future__ import annotations
 
@@ -70,6 +72,10 @@ class HostPipeline:
         # slots are taken in turn across calls, so that with more slots than chunks a call's
         # copies in need not wait for the previous call's read-backs from the same slots
         self.next_slot = 0
+        # run_deferred: the slot holding each chunk's previous block (None before the first call), and
+        # per slot the event after which no later kernel reads it as a previous block
+        self.prev_slot: List[Optional[int]] = [None] * self.chunks
+        self.prev_read: List[Optional[torch.cuda.Event]] = [None] * self.nslots
 
     def _h2d(self, dst: torch.Tensor, src: torch.Tensor) -> None:
         """Host -> device on the copy-in stream: page-locked sources are read
@@ -118,6 +124,85 @@ class HostPipeline:
                 freed = torch.cuda.Event()
                 freed.record(self.s_out)
                 self.freed[k] = freed
+
+
+    def run_deferred(self, accept_len_prev: torch.Tensor, x: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                     dt: torch.Tensor, y: torch.Tensor) -> None:
+        """Enqueue one layer-call in the serving order (``ssm_commit_verify``):
+        commit the previous call's block up to ``accept_len_prev`` (host
+        int32 [batch]; ignored on the first call, which only verifies), then
+        verify the new block (host x, B, C, dt) from the committed state and
+        copy its y to the host. The previous block's x, B and dt are not sent
+        again: they stay in the device staging slots the previous call filled,
+        which needs at least twice as many slots as chunks. Asynchronous, like
+        :meth:`run`; :meth:`finish` commits the last block. Do not interleave
+        :meth:`run` calls before :meth:`finish`: they take the slots in turn
+        and would overwrite the kept block."""
+        if self.nslots < 2 * self.chunks:
+            raise ValueError("run_deferred needs at least twice as many staging slots as chunks")
+        for c in range(self.chunks):
+            lo, hi = self.bounds[c], self.bounds[c + 1]
+            n = hi - lo
+            if n == 0:
+                continue
+            k = self.next_slot
+            self.next_slot = (self.next_slot + 1) % self.nslots
+            kp = self.prev_slot[c]
+            with torch.cuda.stream(self.s_in):
+                for ev in (self.freed[k], self.prev_read[k]):  # its y is out, and no kernel still reads it
+                    if ev is not None:
+                        self.s_in.wait_event(ev)
+                pairs = ((self.slot_x[k][:n], x[lo:hi]), (self.slot_B[k][:n], B[lo:hi]),
+                         (self.slot_C[k][:n], C[lo:hi]), (self.slot_dt[k][:n], dt[lo:hi]),
+                         (self.slot_acc[k][:n], accept_len_prev[lo:hi]))
+                if all(src.is_pinned() and src.is_contiguous() for _, src in pairs):
+                    sv.copy_from_host_n(pairs, stream=self.s_in)
+                else:
+                    for dst, src in pairs:
+                        self._h2d(dst, src)
+                arrived = torch.cuda.Event()
+                arrived.record(self.s_in)
+            with torch.cuda.stream(self.s_k):
+                self.s_k.wait_event(arrived)
+                if kp is None:
+                    sv.verify(self.state[lo:hi], self.slot_x[k][:n], self.slot_B[k][:n], self.slot_C[k][:n],
+                              self.slot_dt[k][:n], self.A, self.D, y=self.slot_y[k][:n], dev_status=self.status,
+                              stream=self.s_k)
+                else:
+                    sv.commit_verify(self.state[lo:hi], self.slot_x[kp][:n], self.slot_B[kp][:n],
+                                     self.slot_dt[kp][:n], self.slot_acc[k][:n], self.slot_x[k][:n],
+                                     self.slot_B[k][:n], self.slot_C[k][:n], self.slot_dt[k][:n], self.A, self.D,
+                                     y=self.slot_y[k][:n], dev_status=self.status, stream=self.s_k)
+                done = torch.cuda.Event()
+                done.record(self.s_k)
+                if kp is not None:
+                    self.prev_read[kp] = done
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(done)
+                y[lo:hi].copy_(self.slot_y[k][:n], non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(self.s_out)
+                self.freed[k] = freed
+            self.prev_slot[c] = k
+
+    def finish(self, accept_len_last: torch.Tensor) -> None:
+        """Commit the last block enqueued by :meth:`run_deferred` up to
+        ``accept_len_last`` (host int32 [batch]) and forget it: the next
+        :meth:`run_deferred` starts with a verify only."""
+        for c in range(self.chunks):
+            lo, hi = self.bounds[c], self.bounds[c + 1]
+            n, kp = hi - lo, self.prev_slot[c]
+            if n == 0 or kp is None:
+                continue
+            acc = self.slot_acc[kp][:n]
+            with torch.cuda.stream(self.s_k):
+                acc.copy_(accept_len_last[lo:hi], non_blocking=True)
+                sv.commit(self.state[lo:hi], self.slot_x[kp][:n], self.slot_B[kp][:n], self.slot_dt[kp][:n],
+                          self.A, acc, dev_status=self.status, stream=self.s_k)
+                done = torch.cuda.Event()
+                done.record(self.s_k)
+                self.prev_read[kp] = done
+            self.prev_slot[c] = None
 
 
 def capture_step(pipelines, inputs, device=None, repeat: int = 1) -> torch.cuda.CUDAGraph:

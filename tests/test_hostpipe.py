@@ -74,6 +74,56 @@ def test_captured_step_equals_device_calls(cuda_device):
             assert torch.equal(pipes[layer].state, st_ref), (rnd, layer)
 
 
+
+@pytest.mark.parametrize("chunks,slots", [(3, None), (2, 5)])
+def test_deferred_pipeline_equals_device_calls(cuda_device, chunks, slots):
+    """run_deferred over five rounds equals, bit for bit, the device calls of
+    the serving order: verify the first block, then commit_verify (previous
+    block up to its accept_len, new block) each round, and finish() the same
+    as a final commit."""
+    dev = cuda_device
+    wl = synth.custom_workload(11, 8, 64, 128, 2, 6, synth.BF16, seed=93)
+    p = synth.draw_params(wl)
+    st_ref = p["state0"].to(dev)
+    st = st_ref.clone()
+    A, D = p["A"].to(dev), p["D"].to(dev)
+    pipe = HostPipeline(st, A, D, wl.ntok, wl.ngroups, torch.bfloat16, chunks=chunks, slots=slots)
+    rounds = 5
+    toks = [synth.draw_tokens(wl, r) for r in range(rounds)]
+    accs = [synth.draw_accept_len(wl, r) for r in range(rounds)]
+    for r in range(rounds):
+        td = to_dev(toks[r], dev)
+        if r == 0:
+            y_ref = ssm.verify(st_ref, td["x"], td["B"], td["C"], td["dt"], A, D)
+        else:
+            pd = to_dev(toks[r - 1], dev)
+            y_ref = ssm.commit_verify(st_ref, pd["x"], pd["B"], pd["dt"], accs[r - 1].to(dev), td["x"], td["B"],
+                                      td["C"], td["dt"], A, D)
+        h = {k: v.pin_memory() for k, v in toks[r].items()}
+        prev_acc = (accs[r - 1] if r > 0 else torch.zeros(wl.batch, dtype=torch.int32)).pin_memory()
+        y = torch.full((wl.batch, wl.ntok, wl.nheads, wl.headdim), float("nan")).pin_memory()
+        pipe.run_deferred(prev_acc, h["x"], h["B"], h["C"], h["dt"], y)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref.cpu()), r
+        assert torch.equal(st, st_ref), r
+    last = to_dev(toks[-1], dev)
+    ssm.commit(st_ref, last["x"], last["B"], last["dt"], A, accs[-1].to(dev))
+    pipe.finish(accs[-1].pin_memory())
+    torch.cuda.synchronize()
+    assert torch.equal(st, st_ref)
+    assert int(pipe.status.item()) == 0
+
+
+def test_deferred_pipeline_needs_two_slots_per_chunk(cuda_device):
+    wl = synth.custom_workload(4, 2, 64, 64, 1, 3, synth.BF16, seed=94)
+    p = synth.draw_params(wl)
+    pipe = HostPipeline(p["state0"].to(cuda_device), p["A"].to(cuda_device), p["D"].to(cuda_device), wl.ntok,
+                        wl.ngroups, torch.bfloat16, chunks=2, slots=3)
+    t = {k: v.pin_memory() for k, v in synth.draw_tokens(wl, 0).items()}
+    y = torch.zeros(wl.batch, wl.ntok, wl.nheads, wl.headdim).pin_memory()
+    with pytest.raises(ValueError):
+        pipe.run_deferred(torch.zeros(wl.batch, dtype=torch.int32).pin_memory(), t["x"], t["B"], t["C"], t["dt"], y)
+
 @pytest.mark.parametrize("nbytes,offset", [(1, 0), (15, 0), (16, 0), (4096 + 7, 0), (6 << 20, 0), (100003, 3)])
 def test_copy_from_host(cuda_device, nbytes, offset):
     """SM-driven copies from page-locked memory: exact bytes for aligned and
